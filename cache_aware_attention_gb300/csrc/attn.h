@@ -1,0 +1,36 @@
+// Internal launch interface of the attention kernels (host + device visible).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mar {
+
+// One attention launch: for every (b, h) the queries Q[bh, 0..nq) attend over a key
+// list made of
+//   - the dense rows Kd/Vd[bh, 0..n_dense)                (fresh K_A/V_A, or all of K/V),
+//   - followed, when idx != nullptr, by the cache rows Kc/Vc[bh, p] for every
+//     position p in [0, N) that is not in idx[b, 0..A)  (the cached set, ascending).
+// Full attention: Kd/Vd = K/V with n_dense = N, idx = nullptr.
+// Cache-aware attention: Kd/Vd = K_A/V_A with n_dense = A, idx = active positions.
+struct AttnParams {
+    const void *Q;      // [B*H, nq, d]
+    const void *Kd;     // [B*H, n_dense, d]
+    const void *Vd;
+    void *Kc;           // [B*H, N, d] cache (written at active rows when fuse_scatter)
+    void *Vc;
+    const int32_t *idx; // [B, A] active positions, or nullptr
+    void *O;            // [B*H, nq, d]
+    float *lse;         // [B*H, nq] natural-log LSE, or nullptr
+    uint32_t *status;
+    int B, H, N, d;
+    int nq, n_dense, A;
+    int fuse_scatter;
+    float scale;        // softmax scale
+};
+
+// Launchers. Return the cudaError_t of the launch.
+cudaError_t launch_attn_f32(const AttnParams &p, cudaStream_t s);
+cudaError_t launch_attn_bf16_mma(const AttnParams &p, cudaStream_t s);
+
+}  // namespace mar

@@ -1,0 +1,137 @@
+// Device-side helpers shared by the library's kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "marattn.h"
+
+#define MAR_DEVINL __device__ __forceinline__
+
+namespace mar {
+
+using bf16 = __nv_bfloat16;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ---------------------------------------------------------------- status word
+MAR_DEVINL void report(uint32_t *status, uint32_t bits) {
+    if (status) atomicOr(status, bits);
+}
+
+// ---------------------------------------------------------------- element conversion
+template <typename T> MAR_DEVINL float to_f32(T x);
+template <> MAR_DEVINL float to_f32<float>(float x) { return x; }
+template <> MAR_DEVINL float to_f32<bf16>(bf16 x) { return __bfloat162float(x); }
+
+MAR_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// ---------------------------------------------------------------- cp.async (16 B)
+MAR_DEVINL uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Copies 16 bytes global -> shared; src_bytes < 16 zero-fills the remainder.
+MAR_DEVINL void cp_async16(void *smem_dst, const void *gmem_src, int src_bytes = 16) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(smem_dst)),
+                 "l"(gmem_src), "r"(src_bytes));
+}
+MAR_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N> MAR_DEVINL void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// ---------------------------------------------------------------- ldmatrix / mma.sync
+MAR_DEVINL void ldmatrix_x4(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3,
+                            const void *smem_row_ptr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32(smem_row_ptr)));
+}
+MAR_DEVINL void ldmatrix_x4_trans(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3,
+                                  const void *smem_row_ptr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32(smem_row_ptr)));
+}
+
+// D = A(16x16 bf16, row) * B(16x8 bf16, col) + D, fp32 accumulate.
+MAR_DEVINL void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Hardware base-2 exponential (PTX ex2.approx); ex2(-inf) = +0.
+MAR_DEVINL float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ---------------------------------------------------------------- active/cached partition
+// Builds, in shared memory, the ascending list of positions of one batch row that are
+// NOT in idx[0..A) (the cached set), using a bitmap of N bits. All threads of the
+// block must call it. Returns the cached count C. Reports out-of-range and repeated
+// positions through `status`; such entries are ignored.
+// bitmap: ceil(N/32) words; cached: N ints; warp_tot: blockDim/32 ints.
+MAR_DEVINL int build_cached_list(const int32_t *__restrict__ idx, int A, int N,
+                                 uint32_t *bitmap, int32_t *cached, int32_t *warp_tot,
+                                 uint32_t *status) {
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int words = (N + 31) >> 5;
+    for (int w = tid; w < words; w += nthr) bitmap[w] = 0u;
+    __syncthreads();
+    uint32_t bad = 0;
+    for (int a = tid; a < A; a += nthr) {
+        int p = idx[a];
+        if (p < 0 || p >= N) {
+            bad |= MAR_STATUS_INDEX_RANGE;
+            continue;
+        }
+        uint32_t old = atomicOr(&bitmap[p >> 5], 1u << (p & 31));
+        if (old & (1u << (p & 31))) bad |= MAR_STATUS_INDEX_DUP;
+    }
+    if (bad) report(status, bad);
+    __syncthreads();
+    const int lane = tid & 31, warp = tid >> 5, nwarp = nthr >> 5;
+    int base = 0;
+    for (int p0 = 0; p0 < N; p0 += nthr) {
+        int p = p0 + tid;
+        bool is_cached = (p < N) && !((bitmap[p >> 5] >> (p & 31)) & 1u);
+        uint32_t ball = __ballot_sync(0xffffffffu, is_cached);
+        int within = __popc(ball & ((1u << lane) - 1u));
+        if (lane == 0) warp_tot[warp] = __popc(ball);
+        __syncthreads();
+        int off = base;
+        for (int w = 0; w < warp; ++w) off += warp_tot[w];
+        if (is_cached) cached[off + within] = p;
+        int tot = 0;
+        for (int w = 0; w < nwarp; ++w) tot += warp_tot[w];
+        base += tot;
+        __syncthreads();
+    }
+    return base;
+}
+
+// Raises the dynamic shared memory limit of `func` to `bytes` once per device.
+template <typename F>
+inline cudaError_t ensure_smem(F *func, size_t bytes, int *configured /* [64] */) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64 && configured[dev] >= (int)bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess && dev < 64) configured[dev] = (int)bytes;
+    return e;
+}
+
+}  // namespace mar

@@ -1,0 +1,50 @@
+// Internal launch interface of the layer-2 score, top-K, row-copy and guidance kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mar {
+
+struct ScoreParams {
+    const void *Q;          // [B*H, N, d] (layer-2 queries of all tokens)
+    const void *K;          // [B*H, N, d]
+    const int32_t *gen;     // [B, G] generating positions
+    double *partial;        // workspace [B*H, N]: per-head sum over g of softmax weights
+    float *score;           // [B, N]
+    uint32_t *status;
+    int B, H, N, d, G;
+    int bf16;               // element type of Q/K
+    float scale;
+};
+
+size_t score_smem_bytes(int N, int d);
+cudaError_t launch_score(const ScoreParams &p, cudaStream_t s);
+
+struct TopkParams {
+    const float *score;     // [B, N]
+    const int32_t *exclude; // [B, E] or nullptr
+    int32_t *out;           // [B, K] or nullptr
+    int32_t *active;        // [B, E + K] or nullptr
+    uint32_t *status;
+    int B, N, E, K;
+};
+
+cudaError_t launch_topk(const TopkParams &p, cudaStream_t s);
+
+struct RowCopyParams {
+    const void *src[3];
+    void *dst[3];
+    int n_tensors;
+    const int32_t *idx;     // [B, A] positions, or nullptr for the identity map (A == N)
+    uint32_t *status;
+    int B, H, N, A;
+    int row_bytes;          // multiple of 16
+    int scatter;            // 1: dst[bh, idx] = src[bh, a]; 0: dst[bh, a] = src[bh, idx]
+};
+
+cudaError_t launch_rows(const RowCopyParams &p, cudaStream_t s);
+cudaError_t launch_cfg(int mode, int64_t n, const float *cond, float *uncond, float *residual,
+                       float w, float *guided, cudaStream_t s);
+
+}  // namespace mar

@@ -1,0 +1,211 @@
+/*
+ * marattn.h -- C ABI of the cache-aware attention library for masked-autoregressive
+ * (MAR) image decoding on GB300 (sm_103a).
+ *
+ * The library implements the per-step hot path of MARché-style decoding:
+ * full bidirectional attention with the layer-2 relevance score, top-K refresh
+ * selection, split active/cached attention merged by online softmax, the KV-cache
+ * gather/scatter, and LazyMAR's condition-cache guidance update.
+ *
+ * Sources, cited by page title and section:
+ *  [M] "MARché: Fast Masked Autoregressive Image Generation with Cache-Aware
+ *      Attention" (paper notes): Method / Overall Architecture; Key Designs 1-3.
+ *  [R] "MARch'e: ... Cache-Aware Attention" (machine review): "What carries the
+ *      argument"; "Assumptions & free parameters" (Appendix A equivalence).
+ *  [L] "LazyMAR: Accelerating Masked Autoregressive Models via Feature Caching"
+ *      (paper notes): Key Designs, Condition Cache.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Pointers are caller-owned DEVICE pointers unless stated otherwise. The
+ *    library never allocates device memory and keeps no state between calls.
+ *  - Tensors are dense and contiguous in the layouts given below:
+ *      Q, K, V, O, cache           [B, H, N, d]   (token rows of d elements)
+ *      Q_A, K_A, V_A, O_A          [B, H, A, d]   (active rows, in idx order)
+ *      active_idx                  [B, A] int32   (token positions in [0, N))
+ *    B counts rows after classifier-free-guidance doubling.
+ *  - Element type: MAR_BF16 (bf16 storage, fp32 accumulation, bf16 output) or
+ *    MAR_F32 (fp32 throughout). Supported head dims d: 32, 64, 80, 128.
+ *  - Alignment: every Q/K/V/O/cache pointer must be 16-byte aligned
+ *    (MAR_ERR_ALIGN); fp32 score/lse arrays need their natural 4-byte alignment.
+ *  - Streams: every call is asynchronous on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream). Argument errors are detected on the host and
+ *    returned before anything is launched.
+ *  - Device-detected errors set bits in the caller's `d_status` word (a device
+ *    uint32 that the caller zeroes; may be NULL to skip reporting): a position
+ *    out of [0, N) (all calls that take positions) or repeated within one row
+ *    (attention calls). The offending access is skipped and the outputs that
+ *    depend on it are unspecified. Kernels never trap.
+ *  - Returns MAR_OK (0) or a negative mar_result.
+ */
+#ifndef MARATTN_H
+#define MARATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *mar_stream_t; /* same object as cudaStream_t */
+
+enum mar_dtype { MAR_F32 = 0, MAR_BF16 = 1 };
+
+enum mar_result {
+    MAR_OK = 0,
+    MAR_ERR_ARG = -1,       /* NULL pointer, negative count, K > candidates, ... */
+    MAR_ERR_SHAPE = -2,     /* unsupported head dim or size limit exceeded */
+    MAR_ERR_DTYPE = -3,     /* unknown element type */
+    MAR_ERR_ALIGN = -4,     /* pointer not 16-byte aligned */
+    MAR_ERR_WORKSPACE = -5, /* workspace NULL, too small or misaligned */
+    MAR_ERR_CUDA = -6,      /* a CUDA call failed; see mar_last_cuda_error() */
+    MAR_ERR_NODEV = -7      /* no usable sm_103 device */
+};
+
+/* Bits OR-ed into *d_status by the kernels. */
+#define MAR_STATUS_INDEX_RANGE 0x1u /* a position outside [0, N) */
+#define MAR_STATUS_INDEX_DUP 0x2u   /* a position repeated within one row */
+
+enum mar_cfg_mode { MAR_CFG_APPLY = 0, MAR_CFG_UPDATE = 1 };
+
+typedef struct mar_shape {
+    int32_t B;     /* batch rows (after CFG doubling) */
+    int32_t H;     /* heads */
+    int32_t N;     /* tokens per row (buffer + image tokens) */
+    int32_t d;     /* head dim: 32, 64, 80 or 128 */
+    int32_t dtype; /* enum mar_dtype */
+} mar_shape;
+
+/* Human-readable text for a mar_result (static storage). */
+const char *mar_error_string(int code);
+/* cudaError_t of the last failed CUDA call on this thread (0 if none). */
+int mar_last_cuda_error(void);
+/* ABI version of this header: major * 10000 + minor * 100 + patch. */
+int mar_version(void);
+
+/*
+ * mar_attn_full -- full bidirectional softmax attention, optionally with the
+ * layer-2 head-averaged relevance score.
+ *
+ * [M] Overall Architecture: layers 1-2 run standard full attention at every
+ * step (and all layers on a full-refresh step, Key Design 3). For each (b, h, i):
+ *   O[b,h,i,:] = sum_j softmax_j(scale * <Q[b,h,i,:], K[b,h,j,:]>) V[b,h,j,:]
+ *   lse[b,h,i] = log sum_j exp(scale * <Q[b,h,i,:], K[b,h,j,:]>)   (natural log)
+ * [M] Key Design 1: the weights from the G generating queries to every token,
+ * averaged over heads (and over the generating queries):
+ *   score[b,j] = 1/(H*G) * sum_h sum_g softmax_j(scale * <Q[b,h,gen[b,g],:], K[b,h,j,:]>)
+ * The score is evaluated to about 1e-7 relative (fp32 products, fp64 sums) so
+ * that the top-K built on it matches an exact evaluation except on near-ties.
+ *
+ *  Q, K, V, O  [B,H,N,d] (dtype); O may not alias Q, K or V.
+ *  scale       softmax scale; 0 selects 1/sqrt(d).
+ *  gen_idx     [B,G] int32 generating positions, or NULL when score_out is NULL.
+ *  score_out   [B,N] fp32 or NULL. Requires G >= 1.
+ *  lse_out     [B,H,N] fp32 or NULL.
+ *  workspace   device scratch of mar_attn_full_workspace_bytes() bytes (256-byte
+ *              aligned), or NULL when that size is 0. Contents are overwritten;
+ *              calls that overlap on the GPU must not share it.
+ */
+size_t mar_attn_full_workspace_bytes(const mar_shape *shape, int32_t G, int want_score);
+int mar_attn_full(const mar_shape *shape, const void *Q, const void *K, const void *V,
+                  void *O, float scale, const int32_t *gen_idx, int32_t G,
+                  float *score_out, float *lse_out, void *workspace,
+                  size_t workspace_bytes, uint32_t *d_status, mar_stream_t stream);
+
+/*
+ * mar_attn_cache_aware -- split attention of the active queries over fresh
+ * active K/V and stored cached K/V, merged with the safe online-softmax rule.
+ *
+ * [M] Key Design 2 and [R] "What carries the argument": with C(b) the positions
+ * of row b that are NOT in active_idx[b] (the cached set; the two sets are
+ * disjoint), each active query i attends over the key list
+ *   K_A[b,h,0..A) followed by K_cache[b,h,p,:] for p in C(b)
+ * (V likewise) as two partial softmax sums merged by running max and running
+ * sum:  z_i = (alpha^(A) V_A + alpha^(C) V_C) / l_i. Cache rows at active
+ * positions hold stale values and are never read. The result equals full
+ * attention over the concatenated list ([R] Appendix A equivalence).
+ *
+ *  Q_A, K_A, V_A, O_A  [B,H,A,d]; active_idx [B,A] distinct positions in [0,N).
+ *  K_cache, V_cache    [B,H,N,d]. Read at cached positions; when fuse_scatter is
+ *                      1 the call also writes K_A/V_A into the rows at the
+ *                      active positions (the mar_kv_scatter update), which no
+ *                      query of the call reads.
+ *  lse_out             [B,H,A] fp32 or NULL.
+ *  A == 0 is a no-op. A == N (no cached tokens) is plain attention over K_A.
+ *  Limit: N <= 16384.
+ */
+size_t mar_attn_cache_aware_workspace_bytes(const mar_shape *shape, int32_t A);
+int mar_attn_cache_aware(const mar_shape *shape, int32_t A, const void *Q_A,
+                         const void *K_A, const void *V_A, void *K_cache, void *V_cache,
+                         const int32_t *active_idx, void *O_A, float scale,
+                         float *lse_out, int32_t fuse_scatter, void *workspace,
+                         size_t workspace_bytes, uint32_t *d_status,
+                         mar_stream_t stream);
+
+/*
+ * mar_kv_scatter -- write refreshed K/V rows into the per-layer cache.
+ *
+ * [M] Key Design 2: active tokens carry fresh K/V; the cache keeps every
+ * token's latest projection. Key Design 3: a full-refresh step overwrites all.
+ *   K_cache[b,h,active_idx[b,a],:] = K_A[b,h,a,:]   (V likewise; bit copies)
+ * active_idx == NULL with A == N overwrites every row in order (full refresh).
+ * Either the K pair or the V pair may be NULL to skip that tensor. Repeated
+ * positions leave it unspecified which row lands.
+ */
+int mar_kv_scatter(const mar_shape *shape, int32_t A, const void *K_A, const void *V_A,
+                   const int32_t *active_idx, void *K_cache, void *V_cache,
+                   uint32_t *d_status, mar_stream_t stream);
+
+/*
+ * mar_kv_gather -- copy the active rows of up to 3 full tensors into dense
+ * active blocks (the active-token gather that feeds the fresh projections).
+ *   dst[t][b,h,a,:] = src[t][b,h,active_idx[b,a],:]   for t < n_tensors (bit copies)
+ * src and dst are HOST arrays of n_tensors (1..3) device pointers.
+ */
+int mar_kv_gather(const mar_shape *shape, int32_t A, int32_t n_tensors,
+                  const void *const *src, void *const *dst, const int32_t *active_idx,
+                  uint32_t *d_status, mar_stream_t stream);
+
+/*
+ * mar_refresh_topk -- choose the refreshing tokens and build the active set.
+ *
+ * [M] Key Design 1: the K tokens with the highest layer-2 relevance score,
+ * excluding the generating and just-decoded tokens (exclude_idx, which are
+ * active anyway), become the refreshing tokens. Equal scores go to the lower
+ * position (scores are ordered by their fp32 bit pattern, so -0 < +0).
+ *  score        [B,N] fp32.
+ *  exclude_idx  [B,E] int32 (E may be 0, then NULL is allowed).
+ *  out_idx      [B,K] int32: the chosen positions in ascending order (or NULL).
+ *  active_out   [B,E+K] int32: exclude_idx[b] followed by out_idx[b] -- the
+ *               active set [generating, just-decoded, refreshing] (or NULL).
+ * Errors: K > N - E returns MAR_ERR_ARG. Limits: N <= 8192.
+ */
+int mar_refresh_topk(int32_t B, int32_t N, const float *score, const int32_t *exclude_idx,
+                     int32_t E, int32_t K, int32_t *out_idx, int32_t *active_out,
+                     uint32_t *d_status, mar_stream_t stream);
+
+/*
+ * mar_cfg_residual -- LazyMAR condition cache on fp32 outputs of n elements.
+ *
+ * [L] Condition Cache: a cached step runs only the conditional branch and
+ * takes uncond = cond - residual (MAR_CFG_APPLY: writes uncond); a full step
+ * runs both branches and refreshes residual = cond - uncond (MAR_CFG_UPDATE:
+ * writes residual). If `guided` is non-NULL it also receives textbook guidance
+ * uncond + w * (cond - uncond) (not printed on the pages). IEEE round-to-
+ * nearest fp32 operations, no fused multiply-add.
+ */
+int mar_cfg_residual(int32_t mode, int64_t n, const float *cond, float *uncond,
+                     float *residual, float w, float *guided, mar_stream_t stream);
+
+/*
+ * mar_status_read -- synchronise `stream` and copy *d_status to *h_status
+ * (host pointer).
+ */
+int mar_status_read(const uint32_t *d_status, uint32_t *h_status, mar_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MARATTN_H */

@@ -1,0 +1,112 @@
+"""The C-ABI library loads and exports every entry point its header declares (CPU only).
+
+Also checks host-side argument validation, which returns before any CUDA work, so
+no GPU is needed: the pointers passed are never dereferenced on those paths.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import cache_aware_attention_gb300 as mar
+from cache_aware_attention_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(mar_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return mar.load()
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ["mar_attn_full", "mar_attn_cache_aware", "mar_kv_scatter", "mar_kv_gather",
+              "mar_refresh_topk", "mar_cfg_residual", "mar_status_read"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(_build.LIB)
+    missing = [n for n in _declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_version_and_error_strings(lib):
+    assert mar.mar_version() >= 10000
+    for code in range(0, -8, -1):
+        assert mar.mar_error_string(code)
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null address that host validation never dereferences
+
+
+def _shape(B=2, H=2, N=64, d=64, dtype=1):
+    return ctypes.byref(mar.MarShape(B, H, N, d, dtype))
+
+
+def test_attn_full_validation(lib):
+    P = ctypes.c_void_p
+    args = lambda s, q=FAKE, ws=None, wb=0, gen=None, G=0, score=None: (
+        s, P(q), P(FAKE), P(FAKE), P(FAKE), ctypes.c_float(0), P(gen), G, P(score), None, P(ws), wb,
+        None, None)
+    assert lib.mar_attn_full(*args(_shape(d=48))) == -2          # unsupported head dim
+    assert lib.mar_attn_full(*args(_shape(dtype=7))) == -3       # unknown dtype
+    assert lib.mar_attn_full(*args(_shape(), q=0)) == -1          # NULL Q
+    assert lib.mar_attn_full(*args(_shape(), q=FAKE + 8)) == -4   # misaligned
+    assert lib.mar_attn_full(*args(_shape(), score=FAKE, G=0, gen=FAKE)) == -1  # score needs G >= 1
+    # score without workspace
+    assert lib.mar_attn_full(*args(_shape(), score=FAKE, G=4, gen=FAKE)) == -5
+    need = lib.mar_attn_full_workspace_bytes(_shape(), 4, 1)
+    assert need >= 2 * 2 * 64 * 8 and need % 256 == 0
+    assert lib.mar_attn_full(*args(_shape(), score=FAKE, G=4, gen=FAKE, ws=FAKE, wb=need - 1)) == -5
+    assert lib.mar_attn_full(*args(_shape(B=0))) == 0             # empty: no-op
+
+
+def test_cache_aware_validation(lib):
+    P = ctypes.c_void_p
+    def call(s, A, idx=FAKE):
+        return lib.mar_attn_cache_aware(s, A, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(idx),
+                                        P(FAKE), ctypes.c_float(0), None, 0, None, 0, None, None)
+    assert call(_shape(), 0) == 0            # A == 0 is a no-op
+    assert call(_shape(), 65) == -1          # A > N
+    assert call(_shape(), 8, idx=0) == -1    # NULL idx
+    assert call(_shape(d=100), 8) == -2
+    assert call(_shape(N=20000), 8) == -2    # beyond the cached-list limit
+
+
+def test_topk_and_cfg_validation(lib):
+    P = ctypes.c_void_p
+    assert lib.mar_refresh_topk(2, 10, P(FAKE), P(FAKE), 4, 7, P(FAKE), None, None, None) == -1  # K > N-E
+    assert lib.mar_refresh_topk(2, 9000, P(FAKE), P(FAKE), 4, 7, P(FAKE), None, None, None) == -2
+    assert lib.mar_refresh_topk(2, 10, P(FAKE), P(FAKE), 4, 3, None, None, None, None) == -1  # no output
+    assert lib.mar_cfg_residual(5, 10, P(FAKE), P(FAKE), P(FAKE), ctypes.c_float(0), None, None) == -1
+    assert lib.mar_cfg_residual(0, 0, None, None, None, ctypes.c_float(0), None, None) == 0
+
+
+def test_rows_validation(lib):
+    P = ctypes.c_void_p
+    assert lib.mar_kv_scatter(_shape(), 8, P(FAKE), P(FAKE), None, P(FAKE), P(FAKE), None, None) == -1
+    arr = (P * 1)(FAKE)
+    assert lib.mar_kv_gather(_shape(), 8, 4, arr, arr, P(FAKE), None, None) == -1  # n_tensors > 3
+    assert lib.mar_kv_gather(_shape(), 8, 1, arr, arr, None, None, None) == -1     # NULL idx
+
+
+def test_binding_rejects_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(1, 1, 8, 32, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        mar.mar_attn_full(x, x, x)
