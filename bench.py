@@ -1,0 +1,516 @@
+"""Benchmark of the MARché decode-step hot path on the MAR-B-shaped workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mine|reference]
+
+Workload: batch 32 doubled to 64 rows for classifier-free guidance, 12 heads, head
+dim 64, 320 tokens (256 image + 64 buffer), bf16, 4 generating + 4 just-decoded +
+top-32 refresh tokens per cached step. Inputs are seeded synthetic tensors.
+
+One bench step is one decode step through the two layers the hot path changes:
+  cached step  : layer-2 full attention + head-averaged score, top-K refresh and
+                 active-set build, active-row gather of layer 3, cache-aware attention
+                 with fused KV-cache scatter, condition-cache apply (uncond = cond - r);
+  refresh step : (step % 3 == 0) layer-2 and layer-3 full attention, full cache
+                 overwrite, condition-cache update (r = cond - uncond).
+Timed steps continue the schedule after the warm-up steps. The unit is the active
+query token of the cache-aware layer: B'*A per cached step, B'*N per refresh step
+(every token is recomputed), so ``value`` = those tokens over the device time.
+
+Three independent input sets (each with its own KV cache) rotate from step to step;
+one set's step touches ~250 MB and the three together ~760 MB, so no step's inputs
+are left in the 129 MB L2 by the previous step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "cache-aware attn active-query tok/s per layer; HBM GB/s & % roofline, 1 GB300"
+UNIT = "tok/s"
+CONFIG = "mar_b"
+N_SETS = 3
+REFRESH_PERIOD = 3
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo", rank=rank, world_size=ws)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu, self.rows, self.proc = gpu, [], None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = [r for t, r in self.rows if self.t0 and self.t1 and self.t0 <= t <= self.t1] or \
+               [r for _, r in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(rows[0][2]),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- workload
+def host_schedule(cfg, n_steps_pool: int, seed: int):
+    """Generating / just-decoded positions for a pool of steps (host side).
+
+    The single-step workload fixes G = J = 4; positions are drawn from the image
+    tokens, shared between the cond and uncond rows of an image."""
+    out = []
+    for s in range(n_steps_pool):
+        pos = workloads.distinct_positions(cfg.B, cfg.G + cfg.J, cfg.n_buf, cfg.N, seed + s)
+        pos = torch.cat([pos, pos], 0) if cfg.cfg else pos
+        out.append((pos[:, :cfg.G].contiguous(), pos.contiguous()))   # gen, exclude = [gen, just]
+    return out
+
+
+class InputSet:
+    def __init__(self, cfg, s, device):
+        ss = workloads.single_step(cfg, device=device, seed=cfg.seed * 100 + s)
+        self.layer2 = (ss.Q2, ss.K2, ss.V2)
+        self.layer3 = (ss.Q3, ss.K3, ss.V3)
+        self.cache = (ss.Kc, ss.Vc)
+        self.cond, self.uncond, self.residual = ss.cond, ss.uncond, ss.residual
+        sched = host_schedule(cfg, 1, 7000 + 17 * s)
+        self.gen, self.exclude = (x.to(device) for x in sched[0])
+
+    def host_copy(self):
+        """Pinned host copies of the per-step inputs (for the end-to-end leg)."""
+        pin = lambda x: x.detach().to("cpu").pin_memory()
+        return {"layer2": [pin(x) for x in self.layer2], "layer3": [pin(x) for x in self.layer3],
+                "gen": pin(self.gen), "exclude": pin(self.exclude), "cond": pin(self.cond),
+                "residual": pin(self.residual), "uncond": pin(self.uncond)}
+
+
+def bytes_full_attention(cfg):
+    return 4 * cfg.Bp * cfg.H * cfg.N * cfg.d * 2          # Q, K, V read + O write (bf16)
+
+
+def bytes_cache_aware(cfg, A):
+    per_bh = 4 * (cfg.N - A) * cfg.d + 6 * A * cfg.d + 2 * A * cfg.d   # cached K/V, Q/K/V_A, O_A
+    return cfg.Bp * cfg.H * per_bh + cfg.Bp * A * 4
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_mine(args, ws, rank, local):
+    import cache_aware_attention_gb300 as mar
+    from cache_aware_attention_gb300 import _build
+    from cache_aware_attention_gb300.step import DecodeStep, is_full_refresh
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        _build.build()
+    barrier(ws)
+    mar.load()
+    cfg = workloads.CONFIGS[CONFIG]
+    A = cfg.A
+    sets = [InputSet(cfg, s, dev) for s in range(N_SETS)]
+    step = DecodeStep(cfg.Bp, cfg.H, cfg.N, cfg.d, cfg.K, A, device=dev, max_gen=cfg.G)
+    n_cfg = cfg.B * cfg.n_img * cfg.latent
+    stream = torch.cuda.current_stream()
+
+    def one_step(t, s: InputSet):
+        kind = step.run(t, s.layer2, s.layer3, s.cache, s.gen, s.exclude)[0]
+        if kind == "full":
+            mar.mar_cfg_residual(mar.MAR_CFG_UPDATE, s.cond, s.uncond, s.residual)
+        else:
+            mar.mar_cfg_residual(mar.MAR_CFG_APPLY, s.cond, s.uncond, s.residual)
+        return kind
+
+    units = lambda t: cfg.Bp * (cfg.N if is_full_refresh(t) else A)
+    clocks = ClockSampler(local)
+    clocks.start()
+
+    # warm-up (eager), then one CUDA graph per (input set, step kind)
+    W, K = args.warmup, args.steps
+    for t in range(W):
+        one_step(t, sets[t % N_SETS])
+    torch.cuda.synchronize()
+    graphs = {}
+    side = torch.cuda.Stream()
+    for si, s in enumerate(sets):
+        for kind_t in (0, 1):        # step 0 -> refresh kind, step 1 -> cached kind
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                one_step(kind_t, s)
+            graphs[(si, kind_t)] = g
+    torch.cuda.synchronize()
+
+    # timed region: exactly K steps, graph replay
+    barrier(ws)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark("t0")
+    ev0.record()
+    tokens = 0
+    for t in range(W, W + K):
+        graphs[(t % N_SETS, 0 if is_full_refresh(t) else 1)].replay()
+        tokens += units(t)
+    ev1.record()
+    torch.cuda.synchronize()
+    clocks.mark("t1")
+    barrier(ws)
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(ms, ws)
+    total_tokens = tokens * ws
+
+    # per-call durations (eager, events around each C-ABI call on the launching stream)
+    brk = breakdown(args, cfg, sets, step, mar, W, K, is_full_refresh)
+
+    # end to end through the C ABI from pinned host buffers
+    e2e = end_to_end(args, cfg, sets, step, mar, W, K, is_full_refresh, units, dev)
+    clocks.stop()
+
+    peaks = load_peaks()
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    fa = brk["attn_full"]
+    roof = {"bound": "hbm", "kernel": "attn_mma_kernel<64> (full attention, N=320)",
+            "achieved": fa["gbs"], "peak": hbm, "unit": "GB/s",
+            "frac": fa["gbs"] / hbm if fa["gbs"] else None, "traffic": None,
+            "peak_source": "MEASURED_PEAKS.json hbm_gbs" if "hbm_gbs" in peaks else "fallback 6800 GB/s"}
+    cpu = cpu_baseline(cfg, budget_s=args.cpu_seconds) if (rank == 0 and ws == 1 and not args.no_cpu) else None
+    n_launch = sum(launches_per_step(t) for t in range(W, W + K))
+    line = {
+        "metric": METRIC, "value": total_tokens / (ms_max / 1e3), "unit": UNIT, "n_gpus": ws,
+        "steps": K, "warmup": W, "ms_per_step": ms_max / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "MAR-B-shaped decode step (batch 32 doubled to 64 for CFG, 12 heads, d=64, "
+                               "256+64 tokens, 4 gen + 4 just-decoded + top-32 refresh, full refresh every 3 steps)",
+                   "B_rows": cfg.Bp, "heads": cfg.H, "head_dim": cfg.d, "tokens": cfg.N, "active": A,
+                   "refresh_period": REFRESH_PERIOD,
+                   "steps_full": sum(1 for t in range(W, W + K) if is_full_refresh(t)),
+                   "unit_tokens": "B'*A per cached step, B'*N per refresh step",
+                   "l2": f"{N_SETS} rotating input sets (~{N_SETS * 8 * bytes_full_attention(cfg) // 4 // 2**20} MB "
+                         "total, > L2), no flush", "timing": "CUDA graph replay, events on the stream"},
+        "roofline": roof,
+        "breakdown": brk,
+        "e2e": e2e,
+        "gpu_launches": n_launch,
+        "cpu_baseline": cpu,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def launches_per_step(t):
+    # refresh: attn(L2) + attn(L3) + scatter + cfg = 4; cached: attn + score(2) + topk + gather +
+    # cache-aware + cfg = 7
+    return 4 if t % REFRESH_PERIOD == 0 else 7
+
+
+def breakdown(args, cfg, sets, step, mar, W, K, is_full_refresh):
+    """Average device time of each C-ABI call over K eager steps (events bracket each call)."""
+    names = ["attn_full", "attn_full+score", "topk", "gather", "cache_aware", "scatter_all", "cfg"]
+    acc = {n: [0.0, 0] for n in names}
+    pairs = []
+    A = cfg.A
+    nstep = min(K, 300)
+
+    def timed(name, fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        pairs.append((name, a, b))
+
+    for t in range(W, W + nstep):
+        s = sets[t % N_SETS]
+        Q2, K2, V2 = s.layer2
+        Q3, K3, V3 = s.layer3
+        Kc, Vc = s.cache
+        if is_full_refresh(t):
+            timed("attn_full", lambda: mar.mar_attn_full(Q2, K2, V2, step.O2))
+            timed("attn_full", lambda: mar.mar_attn_full(Q3, K3, V3, step.O3))
+            timed("scatter_all", lambda: mar.mar_kv_scatter(K3, V3, None, Kc, Vc))
+            timed("cfg", lambda: mar.mar_cfg_residual(mar.MAR_CFG_UPDATE, s.cond, s.uncond, s.residual))
+        else:
+            act = step.active(A)
+            timed("attn_full+score", lambda: mar.mar_attn_full(Q2, K2, V2, step.O2, gen_idx=s.gen,
+                                                               score_out=step.score, workspace=step.workspace))
+            timed("topk", lambda: mar.mar_refresh_topk(step.score, s.exclude, cfg.K, out_idx=step.R,
+                                                       active_out=act))
+            qa, ka, va, oa = (step.dense(i, A) for i in range(4))
+            timed("gather", lambda: mar.mar_kv_gather([Q3, K3, V3], act, dsts=[qa, ka, va]))
+            timed("cache_aware", lambda: mar.mar_attn_cache_aware(qa, ka, va, Kc, Vc, act, O_A=oa,
+                                                                  fuse_scatter=True))
+            timed("cfg", lambda: mar.mar_cfg_residual(mar.MAR_CFG_APPLY, s.cond, s.uncond, s.residual))
+    torch.cuda.synchronize()
+    for n, a, b in pairs:
+        acc[n][0] += a.elapsed_time(b)
+        acc[n][1] += 1
+    algo = {"attn_full": bytes_full_attention(cfg),
+            "attn_full+score": bytes_full_attention(cfg),
+            "topk": cfg.Bp * cfg.N * 4 + cfg.Bp * (cfg.G + cfg.J + cfg.K) * 4,
+            "gather": 2 * 3 * cfg.Bp * cfg.H * A * cfg.d * 2,
+            "cache_aware": bytes_cache_aware(cfg, A) + 2 * cfg.Bp * cfg.H * A * cfg.d * 2,
+            "scatter_all": 4 * cfg.Bp * cfg.H * cfg.N * cfg.d * 2,
+            "cfg": 3 * cfg.B * cfg.n_img * cfg.latent * 4}
+    out = {}
+    for n in names:
+        tot, cnt = acc[n]
+        if cnt == 0:
+            continue
+        us = tot / cnt * 1e3
+        out[n] = {"us": us, "calls": cnt, "bytes": algo[n], "gbs": algo[n] / (us * 1e-6) / 1e9}
+    flops_full = 4 * cfg.Bp * cfg.H * cfg.N * cfg.N * cfg.d
+    if "attn_full" in out:
+        out["attn_full"]["tflops"] = flops_full / (out["attn_full"]["us"] * 1e-6) / 1e12
+    if "cache_aware" in out:
+        out["cache_aware"]["tflops"] = 4 * cfg.Bp * cfg.H * A * cfg.N * cfg.d / (out["cache_aware"]["us"] * 1e-6) / 1e12
+    return out
+
+
+def end_to_end(args, cfg, sets, step, mar, W, K, is_full_refresh, units, dev):
+    """Same metric through the public API with host buffers: every step copies its inputs
+    from pinned host memory and reads its result back."""
+    host = [s.host_copy() for s in sets]
+    A = cfg.A
+    nstep = min(K, 200)
+    res_host = torch.empty(cfg.Bp, cfg.H, A, cfg.d, dtype=torch.bfloat16).pin_memory()
+    full_host = torch.empty(cfg.Bp, cfg.H, cfg.N, cfg.d, dtype=torch.bfloat16).pin_memory()
+    act_host = torch.empty(cfg.Bp, A, dtype=torch.int32).pin_memory()
+    unc_host = torch.empty(cfg.B, cfg.n_img, cfg.latent).pin_memory()
+    h2d = d2h = 0
+    tokens = 0
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for t in range(W, W + nstep):
+        s, h = sets[t % N_SETS], host[t % N_SETS]
+        for dst, src in zip(s.layer2 + s.layer3, h["layer2"] + h["layer3"]):
+            dst.copy_(src, non_blocking=True)
+        s.gen.copy_(h["gen"], non_blocking=True)
+        s.exclude.copy_(h["exclude"], non_blocking=True)
+        s.cond.copy_(h["cond"], non_blocking=True)
+        h2d_step = sum(x.numel() * x.element_size() for x in h["layer2"] + h["layer3"]) + \
+            h["gen"].numel() * 4 + h["exclude"].numel() * 4 + h["cond"].numel() * 4
+        kind = step.run(t, s.layer2, s.layer3, s.cache, s.gen, s.exclude)
+        if kind[0] == "full":
+            mar.mar_cfg_residual(mar.MAR_CFG_UPDATE, s.cond, s.uncond, s.residual)
+            full_host.copy_(kind[1], non_blocking=True)
+            d2h_step = full_host.numel() * 2
+        else:
+            mar.mar_cfg_residual(mar.MAR_CFG_APPLY, s.cond, s.uncond, s.residual)
+            res_host.copy_(kind[1], non_blocking=True)
+            act_host.copy_(kind[2], non_blocking=True)
+            unc_host.copy_(s.uncond, non_blocking=True)
+            d2h_step = res_host.numel() * 2 + act_host.numel() * 4 + unc_host.numel() * 4
+        h2d += h2d_step
+        d2h += d2h_step
+        tokens += units(t)
+    ev1.record()
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    return {"value": tokens / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d // nstep,
+            "d2h_bytes_per_step": d2h // nstep, "steps": nstep}
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+# ----------------------------------------------------------------------------- oracle arm
+def oracle_pairs_step(t, s_host, pairs, cfg):
+    """The oracle's decode step on a sample of (row, head) pairs of one input set.
+    Returns the number of active-query tokens processed (fractional per head)."""
+    import oracle
+    A = cfg.A
+    Q2, K2, V2 = s_host["layer2"]
+    Q3, K3, V3 = s_host["layer3"]
+    Kc, Vc = s_host["cache"]
+    gen, excl = s_host["gen"], s_host["exclude"]
+    done = 0.0
+    by_row = {}
+    for b, h in pairs:
+        by_row.setdefault(b, []).append(h)
+    for b, heads in by_row.items():
+        hs = slice(min(heads), max(heads) + 1)
+        sl = lambda x: x[b:b + 1, hs]
+        if t % REFRESH_PERIOD == 0:
+            oracle.full_attn(sl(Q2), sl(K2), sl(V2))
+            oracle.full_attn(sl(Q3), sl(K3), sl(V3))
+            oracle.scatter(sl(K3), np.arange(cfg.N, dtype=np.int32)[None], sl(Kc))
+            done += len(heads) / cfg.H * cfg.N
+        else:
+            oracle.full_attn(sl(Q2), sl(K2), sl(V2))
+            score = oracle.l2_score(sl(Q2), sl(K2), gen[b:b + 1])
+            R = oracle.topk(score, excl[b:b + 1], cfg.K)
+            act = np.concatenate([excl[b:b + 1].numpy(), R], 1).astype(np.int32)
+            qa, ka, va = (torch.from_numpy(oracle.gather(sl(x), act).view(np.int16).copy())
+                          .view(torch.bfloat16).reshape(1, len(heads), A, cfg.d) for x in (Q3, K3, V3))
+            oracle.cache_aware(qa, ka, va, sl(Kc), sl(Vc), act)
+            oracle.scatter(ka, act, sl(Kc))
+            done += len(heads) / cfg.H * A
+    return done
+
+
+def host_set(cfg, s):
+    ss = workloads.single_step(cfg, device="cpu", seed=cfg.seed * 100 + s)
+    sched = host_schedule(cfg, 1, 7000 + 17 * s)
+    return {"layer2": (ss.Q2, ss.K2, ss.V2), "layer3": (ss.Q3, ss.K3, ss.V3), "cache": (ss.Kc, ss.Vc),
+            "gen": sched[0][0], "exclude": sched[0][1]}
+
+
+def cpu_baseline(cfg, budget_s: float = 12.0):
+    """The oracle, as it stands, on a bounded sample of the same workload."""
+    import oracle
+    oracle.build()
+    s = host_set(cfg.scaled(B=2), 0)         # two images (4 rows) of the same shape
+    pairs = [(b, h) for b in range(4) for h in range(cfg.H)]
+    t0 = time.time()
+    done, t = 0.0, 0
+    while time.time() - t0 < budget_s and t < 64:
+        done += oracle_pairs_step(t, s, pairs, cfg)
+        t += 1
+    el = time.time() - t0
+    return {"value": done / el, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"{t} decode steps (schedule from step 0) of 4 rows x {cfg.H} heads of the same "
+                      f"workload, fp64 C oracle, {el:.1f} s"}
+
+
+def oracle_threads():
+    v = os.environ.get("OMP_NUM_THREADS")
+    return int(v) if v else (os.cpu_count() or 1)
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    cfg = workloads.CONFIGS[CONFIG]
+    s = host_set(cfg.scaled(B=1), 0)
+    Bp = s["layer2"][0].shape[0]
+    all_pairs = [(b, h) for b in range(Bp) for h in range(cfg.H)]
+    # size the per-step sample so the whole run stays within ~2 minutes
+    t0 = time.time()
+    oracle_pairs_step(1, s, all_pairs[:1], cfg)
+    per_pair = max(time.time() - t0, 1e-4)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n_pairs = int(min(len(all_pairs), max(1, budget / per_pair)))
+    pairs = all_pairs[:n_pairs]
+    for t in range(args.warmup):
+        oracle_pairs_step(t, s, pairs, cfg)
+    t0 = time.time()
+    done = 0.0
+    for t in range(args.warmup, args.warmup + args.steps):
+        done += oracle_pairs_step(t, s, pairs, cfg)
+    el = time.time() - t0
+    v = done / el
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "MAR-B-shaped decode step, oracle on a sample of (row, head) pairs per step",
+                       "pairs_per_step": n_pairs},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+                             "sample": f"{n_pairs} (row, head) pairs per step, {args.steps} steps"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_mine(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

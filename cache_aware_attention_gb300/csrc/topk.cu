@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkParams p) {
         const bool sel = c && (keys[j] > T || (eq && eq_rank < take));
         const int slot = out_base + block_excl_scan(sel ? 1 : 0, warp_sums, &tot);
         out_base += tot;
-        if (sel) {
+        if (sel && slot < p.K) {
             if (p.out) p.out[(int64_t)b * p.K + slot] = j;
             if (p.active) p.active[(int64_t)b * (p.E + p.K) + p.E + slot] = j;
         }

@@ -1,0 +1,94 @@
+"""One MARché decode step over the two layers the hot path changes.
+
+MARché notes, Overall Architecture and Key Designs 1-3: at every step the first two
+layers run full attention and layer 2 yields the head-averaged relevance score of the
+generating tokens; the top-K tokens by that score (excluding the generating and
+just-decoded tokens) are refreshed; layers from 3 on run cache-aware attention for the
+active set (generating + just-decoded + refreshing) and write the refreshed K/V back
+into their cache. Key Design 3: step 0 and every step with step % 3 == 0 is a full
+refresh: every layer runs full attention and its whole cache is overwritten.
+
+``DecodeStep`` drives that sequence through the C ABI on one stream: layer 2 stands
+for the always-full layers, layer 3 for the cache-aware layers. It owns the step's
+scratch buffers (allocated once, for the largest active set) and holds no arithmetic:
+the schedule decision is the only logic here.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (mar_attn_cache_aware, mar_attn_full, mar_attn_full_workspace_bytes, mar_kv_gather,
+               mar_kv_scatter, mar_refresh_topk)
+
+REFRESH_PERIOD = 3
+
+
+def is_full_refresh(step: int, period: int = REFRESH_PERIOD) -> bool:
+    """Key Design 3: the initial step and every step with step mod period == 0."""
+    return step % period == 0
+
+
+class DecodeStep:
+    """Buffers and call sequence of one decode step for a batch of B' rows.
+
+    Shapes: fresh Q/K/V of each layer and the layer-3 cache are [B', H, N, d];
+    ``exclude`` is the host schedule's [B', G+J] int32 device tensor (generating then
+    just-decoded positions). ``K`` refresh tokens per row; ``a_max`` bounds G+J+K."""
+
+    def __init__(self, B: int, H: int, N: int, d: int, K: int, a_max: int, dtype=torch.bfloat16,
+                 device="cuda", max_gen: int | None = None):
+        self.B, self.H, self.N, self.d, self.K, self.a_max = B, H, N, d, K, a_max
+        self.device = torch.device(device)
+        dev, f32, i32 = self.device, torch.float32, torch.int32
+        self.score = torch.empty(B, N, dtype=f32, device=dev)
+        self.R = torch.empty(B, K, dtype=i32, device=dev)
+        self._active = torch.empty(B * a_max, dtype=i32, device=dev)
+        self._qkv = [torch.empty(B * H * a_max * d, dtype=dtype, device=dev) for _ in range(3)]
+        self._oa = torch.empty(B * H * a_max * d, dtype=dtype, device=dev)
+        self.O2 = torch.empty(B, H, N, d, dtype=dtype, device=dev)
+        self.O3 = torch.empty(B, H, N, d, dtype=dtype, device=dev)
+        probe = torch.empty(1, 1, 1, d, dtype=dtype, device=dev).expand(B, H, N, d)
+        ws = mar_attn_full_workspace_bytes(probe, max_gen or N, True)
+        self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def active(self, A: int) -> torch.Tensor:
+        return self._active[: self.B * A].view(self.B, A)
+
+    def dense(self, i: int, A: int) -> torch.Tensor:
+        buf = self._oa if i == 3 else self._qkv[i]
+        return buf[: self.B * self.H * A * self.d].view(self.B, self.H, A, self.d)
+
+    def run(self, step: int, layer2, layer3, cache, gen: torch.Tensor, exclude: torch.Tensor,
+            stream=None):
+        """Run one step. ``layer2``/``layer3`` are (Q, K, V); ``cache`` is (K_cache, V_cache).
+
+        Returns ("full", O3 [B',H,N,d]) on a full-refresh step, else
+        ("cached", O_A [B',H,A,d], active [B',A])."""
+        Q2, K2, V2 = layer2
+        Q3, K3, V3 = layer3
+        Kc, Vc = cache
+        if is_full_refresh(step):
+            mar_attn_full(Q2, K2, V2, self.O2, status=self.status, stream=stream)
+            mar_attn_full(Q3, K3, V3, self.O3, status=self.status, stream=stream)
+            mar_kv_scatter(K3, V3, None, Kc, Vc, status=self.status, stream=stream)
+            return ("full", self.O3)
+        A = exclude.shape[1] + self.K
+        act = self.active(A)
+        mar_attn_full(Q2, K2, V2, self.O2, gen_idx=gen, score_out=self.score, workspace=self.workspace,
+                      status=self.status, stream=stream)
+        mar_refresh_topk(self.score, exclude, self.K, out_idx=self.R, active_out=act,
+                         status=self.status, stream=stream)
+        return self.cached_layer(A, layer3, cache, stream=stream)
+
+    def cached_layer(self, A: int, layer3, cache, stream=None):
+        """Gather the active rows of layer 3 and run cache-aware attention with the fused
+        cache scatter, using the active set already in ``active(A)``."""
+        Q3, K3, V3 = layer3
+        Kc, Vc = cache
+        act = self.active(A)
+        qa, ka, va, oa = (self.dense(i, A) for i in range(4))
+        mar_kv_gather([Q3, K3, V3], act, dsts=[qa, ka, va], status=self.status, stream=stream)
+        mar_attn_cache_aware(qa, ka, va, Kc, Vc, act, O_A=oa, fuse_scatter=True, status=self.status,
+                             stream=stream)
+        return ("cached", oa, act)

@@ -1,0 +1,318 @@
+"""GPU parity: every entry point of the C-ABI library against the CPU oracle.
+
+Inputs come from the seeded generators in ``workloads``; expected values come only
+from ``oracle``. Small cases span several tiles and ragged tails; the configs'
+full-size cases run the GPU on the whole batch and compare sampled batch rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import cache_aware_attention_gb300 as mar
+import oracle
+import workloads
+import _parity as P
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from cache_aware_attention_gb300 import _build
+    _build.build()
+    mar.load()
+    oracle.build()
+
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+def _rand(shape, seed, dtype, device=DEV, std=1.0):
+    return workloads.normal(shape, seed, dtype, device, std=std)
+
+
+def _active(B, A, N, seed, lo=0):
+    return workloads.distinct_positions(B, A, lo, N, seed).to(DEV)
+
+
+def _gather_host(x, idx):
+    x = x.detach().cpu()
+    idx = idx.detach().cpu().long()
+    return torch.stack([x[b][:, idx[b]] for b in range(x.shape[0])])
+
+
+DT = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+# ------------------------------------------------------------------------------ full attention
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("B,H,N,d", [(1, 2, 64, 32), (2, 3, 200, 64), (1, 2, 129, 80), (2, 1, 77, 128),
+                                     (1, 1, 1, 64), (2, 2, 320, 64)])
+def test_full_attention(dtype, B, H, N, d):
+    t = DT[dtype]
+    Q, K, V = (_rand((B, H, N, d), 10 + i, t) for i in range(3))
+    lse = torch.empty(B, H, N, dtype=torch.float32, device=DEV)
+    O = mar.mar_attn_full(Q, K, V, lse_out=lse)
+    torch.cuda.synchronize()
+    O_ref, L_ref = oracle.full_attn(Q, K, V)
+    P.assert_close(O, O_ref, dtype, "O")
+    np.testing.assert_allclose(lse.cpu().numpy(), L_ref, atol=1e-5 if dtype == "f32" else 2e-4, rtol=0)
+
+
+def test_full_attention_explicit_scale():
+    Q, K, V = (_rand((1, 2, 96, 64), 20 + i, torch.bfloat16) for i in range(3))
+    O = mar.mar_attn_full(Q, K, V, scale=0.3)
+    O_ref, _ = oracle.full_attn(Q, K, V, scale=0.3)
+    P.assert_close(O, O_ref, "bf16", "O")
+
+
+@pytest.mark.parametrize("name", ["mar_b", "mar_h", "px512"])
+def test_full_attention_config_sampled_rows(name):
+    cfg = workloads.CONFIGS[name]
+    shape = (cfg.Bp, cfg.H, cfg.N, cfg.d)
+    Q, K, V = (_rand(shape, cfg.seed * 100 + i, torch.bfloat16) for i in range(3))
+    O = mar.mar_attn_full(Q, K, V)
+    torch.cuda.synchronize()
+    rows = [0, cfg.Bp - 1] if name != "mar_b" else [0, 17, cfg.Bp - 1]
+    for b in rows:
+        O_ref, _ = oracle.full_attn(Q[b:b + 1], K[b:b + 1], V[b:b + 1])
+        P.assert_close(O[b:b + 1], O_ref, "bf16", f"{name} row {b}")
+
+
+# ------------------------------------------------------------------------------ cache-aware attention
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("B,H,N,A,d", [(1, 2, 64, 8, 32), (2, 3, 300, 70, 64), (2, 2, 320, 40, 80),
+                                        (1, 2, 100, 100, 64), (2, 2, 50, 1, 128), (1, 1, 1088, 114, 80),
+                                        (3, 2, 257, 130, 64)])
+def test_cache_aware_small(dtype, B, H, N, A, d):
+    t = DT[dtype]
+    idx = _active(B, A, N, 30 + A)
+    Q_A, K_A, V_A = (_rand((B, H, A, d), 31 + i, t) for i in range(3))
+    Kc, Vc = _rand((B, H, N, d), 35, t), _rand((B, H, N, d), 36, t)
+    lse = torch.empty(B, H, A, dtype=torch.float32, device=DEV)
+    st = _status()
+    O = mar.mar_attn_cache_aware(Q_A, K_A, V_A, Kc, Vc, idx, lse_out=lse, status=st)
+    assert mar.mar_status_read(st) == 0
+    O_ref, L_ref = oracle.cache_aware(Q_A, K_A, V_A, Kc, Vc, idx)
+    P.assert_close(O, O_ref, dtype, "O_A")
+    np.testing.assert_allclose(lse.cpu().numpy(), L_ref, atol=1e-5 if dtype == "f32" else 2e-4, rtol=0)
+
+
+def test_cache_aware_tiny_config_fp32():
+    cfg = workloads.CONFIGS["tiny"]
+    ss = workloads.single_step(cfg, device="cpu")
+    idx = workloads.distinct_positions(1, cfg.A, 0, cfg.N, 77)
+    QA, KA, VA = _gather_host(ss.Q3, idx), _gather_host(ss.K3, idx), _gather_host(ss.V3, idx)
+    d = lambda x: x.to(DEV).contiguous()
+    O = mar.mar_attn_cache_aware(d(QA), d(KA), d(VA), d(ss.Kc), d(ss.Vc), d(idx))
+    O_ref, _ = oracle.cache_aware(QA, KA, VA, ss.Kc, ss.Vc, idx)
+    P.assert_close(O, O_ref, "f32", "tiny O_A")
+
+
+def test_cache_aware_equals_full_attention_when_cache_current():
+    # The Appendix A equivalence, on the GPU path: current cache -> full attention result.
+    B, H, N, A, d = 2, 4, 320, 40, 64
+    K, V = _rand((B, H, N, d), 41, torch.bfloat16), _rand((B, H, N, d), 42, torch.bfloat16)
+    idx = _active(B, A, N, 43)
+    Q_A = _rand((B, H, A, d), 44, torch.bfloat16)
+    K_A, V_A = mar.mar_kv_gather([K, V], idx)
+    O = mar.mar_attn_cache_aware(Q_A, K_A, V_A, K, V, idx)
+    O_ref, _ = oracle.full_attn(Q_A, K, V)
+    P.assert_close(O, O_ref, "bf16", "O_A vs full")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_cache_aware_fused_scatter_is_bit_exact(dtype):
+    t = DT[dtype]
+    B, H, N, A, d = 3, 2, 200, 37, 64
+    idx = _active(B, A, N, 51)
+    Q_A, K_A, V_A = (_rand((B, H, A, d), 52 + i, t) for i in range(3))
+    Kc, Vc = _rand((B, H, N, d), 55, t), _rand((B, H, N, d), 56, t)
+    Kc0, Vc0 = Kc.clone(), Vc.clone()
+    O = mar.mar_attn_cache_aware(Q_A, K_A, V_A, Kc, Vc, idx, fuse_scatter=True)
+    torch.cuda.synchronize()
+    O_ref, _ = oracle.cache_aware(Q_A, K_A, V_A, Kc0, Vc0, idx)   # reads the pre-scatter cache
+    P.assert_close(O, O_ref, dtype, "O_A")
+    assert np.array_equal(oracle._rows_as_bytes(Kc.cpu()), oracle.scatter(K_A.cpu(), idx.cpu(), Kc0.cpu()))
+    assert np.array_equal(oracle._rows_as_bytes(Vc.cpu()), oracle.scatter(V_A.cpu(), idx.cpu(), Vc0.cpu()))
+
+
+def test_cache_aware_mar_b_full_size():
+    cfg = workloads.CONFIGS["mar_b"]
+    ss = workloads.single_step(cfg, device=DEV)
+    idx = torch.cat([ss.gen, ss.just, _active(cfg.Bp, cfg.K, cfg.N, 61)], 1)
+    # refresh positions drawn apart from gen/just: rebuild rows that collide
+    idx = _distinct_rows(idx, cfg.N, 62)
+    QA, KA, VA = mar.mar_kv_gather([ss.Q3, ss.K3, ss.V3], idx)
+    st = _status()
+    O = mar.mar_attn_cache_aware(QA, KA, VA, ss.Kc, ss.Vc, idx, status=st)
+    assert mar.mar_status_read(st) == 0
+    O_ref, _ = oracle.cache_aware(QA, KA, VA, ss.Kc, ss.Vc, idx)
+    P.assert_close(O, O_ref, "bf16", "MAR-B O_A")
+
+
+def _distinct_rows(idx, N, seed):
+    """Replace repeated positions within a row by unused ones (keeps the first occurrence)."""
+    g = np.random.default_rng(seed)
+    a = idx.cpu().numpy().copy()
+    for b in range(a.shape[0]):
+        seen, free = set(), [p for p in g.permutation(N) if p not in set(a[b].tolist())]
+        for i in range(a.shape[1]):
+            if a[b, i] in seen:
+                a[b, i] = free.pop()
+            seen.add(a[b, i])
+    return torch.from_numpy(a).to(DEV)
+
+
+@pytest.mark.parametrize("A", [6, 16, 32, 64, 96, 160])
+def test_cache_aware_mar_h_sweep_sampled_rows(A):
+    cfg = workloads.CONFIGS["mar_h"]
+    shape = (cfg.Bp, cfg.H, cfg.N, cfg.d)
+    Kc, Vc = _rand(shape, 301, torch.bfloat16), _rand(shape, 302, torch.bfloat16)
+    ashape = (cfg.Bp, cfg.H, A, cfg.d)
+    Q_A, K_A, V_A = (_rand(ashape, 303 + i, torch.bfloat16) for i in range(3))
+    idx = _active(cfg.Bp, A, cfg.N, 310 + A)
+    O = mar.mar_attn_cache_aware(Q_A, K_A, V_A, Kc, Vc, idx)
+    torch.cuda.synchronize()
+    for b in (0, cfg.Bp // 2, cfg.Bp - 1):
+        sl = slice(b, b + 1)
+        O_ref, _ = oracle.cache_aware(Q_A[sl], K_A[sl], V_A[sl], Kc[sl], Vc[sl], idx[sl])
+        P.assert_close(O[sl], O_ref, "bf16", f"MAR-H A={A} row {b}")
+
+
+def test_cache_aware_px512_sampled_rows():
+    cfg = workloads.CONFIGS["px512"]
+    A = 25 + 25 + cfg.K
+    shape = (cfg.Bp, cfg.H, cfg.N, cfg.d)
+    Kc, Vc = _rand(shape, 401, torch.bfloat16), _rand(shape, 402, torch.bfloat16)
+    Q_A, K_A, V_A = (_rand((cfg.Bp, cfg.H, A, cfg.d), 403 + i, torch.bfloat16) for i in range(3))
+    idx = _active(cfg.Bp, A, cfg.N, 410)
+    O = mar.mar_attn_cache_aware(Q_A, K_A, V_A, Kc, Vc, idx)
+    torch.cuda.synchronize()
+    for b in (3, cfg.Bp - 1):
+        sl = slice(b, b + 1)
+        O_ref, _ = oracle.cache_aware(Q_A[sl], K_A[sl], V_A[sl], Kc[sl], Vc[sl], idx[sl])
+        P.assert_close(O[sl], O_ref, "bf16", f"512px row {b}")
+
+
+def test_cache_aware_reports_bad_indices():
+    B, H, N, A, d = 2, 2, 64, 4, 32
+    Q_A = _rand((B, H, A, d), 71, torch.float32)
+    Kc = _rand((B, H, N, d), 72, torch.float32)
+    dup = torch.tensor([[1, 2, 2, 3], [0, 1, 2, 3]], dtype=torch.int32, device=DEV)
+    st = _status()
+    mar.mar_attn_cache_aware(Q_A, Q_A, Q_A, Kc, Kc, dup, status=st)
+    assert mar.mar_status_read(st) & mar.MAR_STATUS_INDEX_DUP
+    bad = torch.tensor([[1, 2, 64, 3], [0, -1, 2, 3]], dtype=torch.int32, device=DEV)
+    st = _status()
+    mar.mar_attn_cache_aware(Q_A, Q_A, Q_A, Kc, Kc, bad, status=st)
+    assert mar.mar_status_read(st) & mar.MAR_STATUS_INDEX_RANGE
+
+
+# ------------------------------------------------------------------------------ gather / scatter
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_gather_and_scatter_bit_exact(dtype):
+    t = DT[dtype]
+    B, H, N, A, d = 4, 3, 321, 45, 80
+    idx = _active(B, A, N, 81)
+    X, Y, Z = (_rand((B, H, N, d), 82 + i, t) for i in range(3))
+    gx, gy, gz = mar.mar_kv_gather([X, Y, Z], idx)
+    for g, full in ((gx, X), (gy, Y), (gz, Z)):
+        assert np.array_equal(oracle._rows_as_bytes(g.cpu()), oracle.gather(full.cpu(), idx.cpu()))
+    Kc, Vc = _rand((B, H, N, d), 90, t), _rand((B, H, N, d), 91, t)
+    K0, V0 = Kc.clone().cpu(), Vc.clone().cpu()
+    KA, VA = _rand((B, H, A, d), 92, t), _rand((B, H, A, d), 93, t)
+    mar.mar_kv_scatter(KA, VA, idx, Kc, Vc)
+    assert np.array_equal(oracle._rows_as_bytes(Kc.cpu()), oracle.scatter(KA.cpu(), idx.cpu(), K0))
+    assert np.array_equal(oracle._rows_as_bytes(Vc.cpu()), oracle.scatter(VA.cpu(), idx.cpu(), V0))
+
+
+def test_full_refresh_overwrite():
+    B, H, N, d = 2, 2, 100, 64
+    K, V = _rand((B, H, N, d), 95, torch.bfloat16), _rand((B, H, N, d), 96, torch.bfloat16)
+    Kc, Vc = torch.zeros_like(K), torch.zeros_like(V)
+    mar.mar_kv_scatter(K, V, None, Kc, Vc)
+    assert np.array_equal(P.bits(Kc), P.bits(K)) and np.array_equal(P.bits(Vc), P.bits(V))
+
+
+def test_scatter_reports_out_of_range():
+    B, H, N, A, d = 1, 1, 16, 2, 32
+    X = _rand((B, H, A, d), 97, torch.float32)
+    C0 = _rand((B, H, N, d), 98, torch.float32)
+    C = C0.clone()
+    st = _status()
+    mar.mar_kv_scatter(X, X, torch.tensor([[3, 99]], dtype=torch.int32, device=DEV), C, C, status=st)
+    assert mar.mar_status_read(st) & mar.MAR_STATUS_INDEX_RANGE
+    assert torch.equal(C[0, 0, 3], X[0, 0, 0])          # the valid row still lands
+    assert torch.equal(C[0, 0, 4:], C0[0, 0, 4:])
+
+
+# ------------------------------------------------------------------------------ score + top-K
+@pytest.mark.parametrize("name,G,K", [("tiny", 2, 4), ("mar_b", 4, 32), ("mar_h", 4, 16), ("mar_h", 4, 64),
+                                      ("px512", 25, 64)])
+def test_score_and_topk(name, G, K):
+    cfg = workloads.CONFIGS[name]
+    rows = cfg.Bp if cfg.Bp <= 64 else 8
+    shape = (rows, cfg.H, cfg.N, cfg.d)
+    Q, Kt, V = (_rand(shape, 500 + i, cfg.torch_dtype) for i in range(3))
+    pos = workloads.distinct_positions(rows, 2 * G, cfg.n_buf, cfg.N, 510).to(DEV)
+    gen, just = pos[:, :G].contiguous(), pos[:, G:].contiguous()
+    score = torch.empty(rows, cfg.N, dtype=torch.float32, device=DEV)
+    st = _status()
+    mar.mar_attn_full(Q, Kt, V, gen_idx=gen, score_out=score, status=st)
+    assert mar.mar_status_read(st) == 0
+    ref = oracle.l2_score(Q, Kt, gen)
+    got = score.cpu().numpy().astype(np.float64)
+    rel = np.abs(got - ref) / ref
+    assert rel.max() < 1e-6, f"score relative error {rel.max():.3g}"
+    excl = torch.cat([gen, just], 1).contiguous()
+    active = torch.empty(rows, 2 * G + K, dtype=torch.int32, device=DEV)
+    R = mar.mar_refresh_topk(score, excl, K, active_out=active)
+    R_np = R.cpu().numpy()
+    # selection logic: bit-exact against the oracle's sort of the SAME fp32 scores
+    assert np.array_equal(R_np, oracle.topk(got, excl.cpu(), K))
+    # end to end against the fp64 scores: exact except near-ties (logged)
+    ties = P.topk_mismatches(R_np, oracle.topk(ref, excl.cpu(), K), ref, excl.cpu().numpy(), K)
+    if ties:
+        print(f"near-ties within {P.TIE_REL:g}: {ties}")
+    assert np.array_equal(active.cpu().numpy(), np.concatenate([excl.cpu().numpy(), R_np], 1))
+
+
+@pytest.mark.parametrize("N,E,K,levels", [(320, 8, 32, 0), (320, 8, 32, 5), (1088, 50, 64, 3), (64, 4, 4, 0),
+                                          (300, 0, 300, 2), (5000, 10, 700, 0), (20, 3, 0, 0)])
+def test_topk_selection_bit_exact(N, E, K, levels):
+    g = np.random.default_rng(N + K)
+    B = 6
+    sc = g.random((B, N)).astype(np.float32)
+    if levels:
+        sc = (np.floor(sc * levels) / levels).astype(np.float32)      # many exact ties
+    sc[0, :5] = [0.0, -0.0, np.inf, 1e-30, 3.0]
+    excl = np.stack([g.permutation(N)[:E] for _ in range(B)]).astype(np.int32).reshape(B, E)
+    score = torch.from_numpy(sc).to(DEV)
+    ex = torch.from_numpy(excl).to(DEV) if E else None
+    out = torch.empty(B, K, dtype=torch.int32, device=DEV)
+    mar.mar_refresh_topk(score, ex, K, out_idx=out)
+    if K:
+        assert np.array_equal(out.cpu().numpy(), oracle.topk(sc.astype(np.float64), excl, K))
+
+
+# ------------------------------------------------------------------------------ condition cache
+@pytest.mark.parametrize("n", [4096 * 16, 1024 * 16 * 64, 1001])
+def test_cfg_residual(n):
+    cond = _rand((n,), 601, torch.float32) * 3
+    res = _rand((n,), 602, torch.float32, std=0.1)
+    unc = torch.empty_like(cond)
+    guided = torch.empty_like(cond)
+    mar.mar_cfg_residual(mar.MAR_CFG_APPLY, cond, unc, res, w=4.0, guided=guided)
+    u_ref, _, g_ref = oracle.cfg(oracle.CFG_APPLY, cond, residual=res, w=4.0)
+    assert np.array_equal(unc.cpu().numpy(), u_ref.astype(np.float32))      # one IEEE subtraction
+    np.testing.assert_allclose(guided.cpu().numpy(), g_ref, rtol=1e-6, atol=1e-6)
+    res2 = torch.empty_like(cond)
+    mar.mar_cfg_residual(mar.MAR_CFG_UPDATE, cond, unc, res2)
+    _, r_ref, _ = oracle.cfg(oracle.CFG_UPDATE, cond, uncond=unc)
+    assert np.array_equal(res2.cpu().numpy(), r_ref.astype(np.float32))
