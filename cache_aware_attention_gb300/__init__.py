@@ -203,7 +203,7 @@ def mar_refresh_topk(score, exclude_idx, K: int, out_idx=None, active_out=None, 
     """Top-K refresh positions [B,K] (ascending) and optional active set [B,E+K]."""
     B, N = score.shape
     E = 0 if exclude_idx is None else int(exclude_idx.shape[1])
-    if out_idx is None and active_out is None:
+    if out_idx is None:
         out_idx = torch.empty(B, K, dtype=torch.int32, device=score.device)
     rc = load().mar_refresh_topk(B, N, _ptr(score), _ptr(exclude_idx), E, int(K), _ptr(out_idx),
                                  _ptr(active_out), _ptr(status), _stream(stream))
