@@ -190,7 +190,7 @@ int mar_refresh_topk(int32_t B, int32_t N, const float *score, const int32_t *ex
     if (E > N || K > N - E) return MAR_ERR_ARG;
     if (B == 0 || N == 0) return MAR_OK;
     if (!score || (E > 0 && !exclude_idx)) return MAR_ERR_ARG;
-    if (!out_idx && !active_out) return MAR_ERR_ARG;
+    if (!out_idx && !active_out) return K == 0 ? MAR_OK : MAR_ERR_ARG;
     mar::TopkParams p{};
     p.score = score; p.exclude = exclude_idx; p.out = out_idx; p.active = active_out;
     p.status = d_status; p.B = B; p.N = N; p.E = E; p.K = K;

@@ -93,6 +93,7 @@ def test_topk_and_cfg_validation(lib):
     assert lib.mar_refresh_topk(2, 10, P(FAKE), P(FAKE), 4, 7, P(FAKE), None, None, None) == -1  # K > N-E
     assert lib.mar_refresh_topk(2, 9000, P(FAKE), P(FAKE), 4, 7, P(FAKE), None, None, None) == -2
     assert lib.mar_refresh_topk(2, 10, P(FAKE), P(FAKE), 4, 3, None, None, None, None) == -1  # no output
+    assert lib.mar_refresh_topk(2, 10, P(FAKE), P(FAKE), 4, 0, None, None, None, None) == 0   # K = 0
     assert lib.mar_cfg_residual(5, 10, P(FAKE), P(FAKE), P(FAKE), ctypes.c_float(0), None, None) == -1
     assert lib.mar_cfg_residual(0, 0, None, None, None, ctypes.c_float(0), None, None) == 0
 
