@@ -8,12 +8,16 @@
 //
 // The refresh set must match an exact evaluation except where two candidates lie within
 // 1e-6 (relative) of each other, so this path is kept well below that error: bf16
-// products are exact in fp32, dot products accumulate in fp32 in a fixed order, the
-// exponentials use the accurate expf, and every sum over keys, generating queries and
-// heads is accumulated in fp64 in a fixed order (deterministic, no atomics).
+// products are exact in fp32, each dot product accumulates in fp32 in a fixed order,
+// the exponentials use the accurate expf, and every sum over keys, generating queries
+// and heads is accumulated in fp64 in a fixed order (deterministic, no atomics).
 //
-// Two kernels: per-(b, h) partial sums over g into a workspace [B, H, N], then a fixed
-// order reduction over h.
+// Kernel 1, one CTA per (b, h): every thread owns keys j = tid, tid + 128, ...; it reads
+// each key row once and forms the logits of up to GCH generating queries at a time
+// (query rows broadcast from shared memory). Each warp then reduces the max and the
+// fp64 exponential sum of one generating query with shuffles, and every thread adds
+// the normalised weights of its keys, g in order, into an fp64 accumulator.
+// Kernel 2: fixed-order sum over heads, divided by H*G.
 #include <cmath>
 
 #include "common.cuh"
@@ -22,93 +26,101 @@
 namespace mar {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int GC = 4;  // generating queries per pass
+constexpr int kThreads = 128;
+constexpr int kWarps = kThreads / 32;
+constexpr int GCH = 8;  // generating queries per pass
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) score_partial_kernel(ScoreParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    double *acc = reinterpret_cast<double *>(smem_raw);        // [N] sum over g of p_gj
-    float *s = reinterpret_cast<float *>(acc + p.N);            // [GC][N] logits
-    float *qs = s + GC * p.N;                                   // [GC][D]
-    double *red = reinterpret_cast<double *>(qs + GC * D);     // [kThreads]
-    float *stat = reinterpret_cast<float *>(red + kThreads);    // [2*GC]: max, 1/l
-    __shared__ int valid[GC];
+    double *acc = reinterpret_cast<double *>(smem_raw);          // [N]
+    float *s = reinterpret_cast<float *>(acc + p.N);              // [GCH][N] logits
+    float *qs = s + GCH * p.N;                                    // [GCH][D]
+    float *stat = qs + GCH * D;                                   // [GCH][2]: max, 1/l
+    __shared__ int valid[GCH];
 
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int bh = blockIdx.x, b = bh / p.H;
     const T *__restrict__ Q = static_cast<const T *>(p.Q);
-    const T *__restrict__ K = static_cast<const T *>(p.K);
-    const T *__restrict__ Kbh = K + (int64_t)bh * p.N * D;
+    const T *__restrict__ Kbh = static_cast<const T *>(p.K) + (int64_t)bh * p.N * D;
 
     for (int j = tid; j < p.N; j += kThreads) acc[j] = 0.0;
 
-    for (int g0 = 0; g0 < p.G; g0 += GC) {
-        const int gn = min(GC, p.G - g0);
-        __syncthreads();
-        if (tid < GC) {
+    for (int g0 = 0; g0 < p.G; g0 += GCH) {
+        const int gn = min(GCH, p.G - g0);
+        __syncthreads();  // previous pass done with s/qs/stat
+        if (tid < GCH) {
             int ok = 0;
             if (tid < gn) {
-                int pos = p.gen[(int64_t)b * p.G + g0 + tid];
+                const int pos = p.gen[(int64_t)b * p.G + g0 + tid];
                 ok = (pos >= 0 && pos < p.N);
                 if (!ok) report(p.status, MAR_STATUS_INDEX_RANGE);
             }
             valid[tid] = ok;
         }
         __syncthreads();
-        for (int t = tid; t < GC * D; t += kThreads) {
-            int g = t / D, c = t % D;
+        for (int t = tid; t < GCH * D; t += kThreads) {
+            const int g = t / D, c = t % D;
             float v = 0.f;
             if (g < gn && valid[g]) {
-                int pos = p.gen[(int64_t)b * p.G + g0 + g];
+                const int pos = p.gen[(int64_t)b * p.G + g0 + g];
                 v = to_f32(Q[((int64_t)bh * p.N + pos) * D + c]);
             }
             qs[t] = v;
         }
         __syncthreads();
-        // logits s[g][j] (fixed accumulation order over c)
+        // logits: one key row per thread, all generating queries of the pass
         for (int j = tid; j < p.N; j += kThreads) {
-            float dot[GC];
+            float dot[GCH];
 #pragma unroll
-            for (int g = 0; g < GC; ++g) dot[g] = 0.f;
+            for (int g = 0; g < GCH; ++g) dot[g] = 0.f;
             const T *kr = Kbh + (int64_t)j * D;
-#pragma unroll 4
-            for (int c = 0; c < D; ++c) {
-                const float kv = to_f32(kr[c]);
+#pragma unroll 2
+            for (int c0 = 0; c0 < D; c0 += 8) {
+                float kv[8];
+                if constexpr (sizeof(T) == 2) {
+                    const uint4 raw = *reinterpret_cast<const uint4 *>(kr + c0);
+                    const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
 #pragma unroll
-                for (int g = 0; g < GC; ++g) dot[g] = fmaf(qs[g * D + c], kv, dot[g]);
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(h2[e]);
+                        kv[2 * e] = f.x;
+                        kv[2 * e + 1] = f.y;
+                    }
+                } else {
+                    const float4 a = *reinterpret_cast<const float4 *>(kr + c0);
+                    const float4 bq = *reinterpret_cast<const float4 *>(kr + c0 + 4);
+                    kv[0] = a.x; kv[1] = a.y; kv[2] = a.z; kv[3] = a.w;
+                    kv[4] = bq.x; kv[5] = bq.y; kv[6] = bq.z; kv[7] = bq.w;
+                }
+#pragma unroll
+                for (int g = 0; g < GCH; ++g) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) dot[g] = fmaf(qs[g * D + c0 + e], kv[e], dot[g]);
+                }
             }
 #pragma unroll
-            for (int g = 0; g < GC; ++g) s[g * p.N + j] = dot[g] * p.scale;
+            for (int g = 0; g < GCH; ++g)
+                if (g < gn) s[g * p.N + j] = dot[g] * p.scale;
         }
         __syncthreads();
-        // per generating query: max and (fp64) sum of exponentials
-        for (int g = 0; g < gn; ++g) {
+        // per generating query (one warp each): max and fp64 sum of exponentials
+        for (int g = warp; g < gn; g += kWarps) {
+            const float *sg = s + g * p.N;
             float mx = -INFINITY;
-            for (int j = tid; j < p.N; j += kThreads) mx = fmaxf(mx, s[g * p.N + j]);
-            red[tid] = (double)mx;
-            __syncthreads();
-            for (int w = kThreads / 2; w > 0; w >>= 1) {
-                if (tid < w) red[tid] = fmax(red[tid], red[tid + w]);
-                __syncthreads();
-            }
-            const float m = (float)red[0];
-            __syncthreads();
+            for (int j = lane; j < p.N; j += 32) mx = fmaxf(mx, sg[j]);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
             double l = 0.0;
-            for (int j = tid; j < p.N; j += kThreads) l += (double)expf(s[g * p.N + j] - m);
-            red[tid] = l;
-            __syncthreads();
-            for (int w = kThreads / 2; w > 0; w >>= 1) {
-                if (tid < w) red[tid] += red[tid + w];
-                __syncthreads();
+            for (int j = lane; j < p.N; j += 32) l += (double)expf(sg[j] - mx);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+            if (lane == 0) {
+                stat[2 * g] = mx;
+                stat[2 * g + 1] = (float)(1.0 / l);
             }
-            if (tid == 0) {
-                stat[2 * g] = m;
-                stat[2 * g + 1] = (float)(1.0 / red[0]);
-            }
-            __syncthreads();
         }
-        // accumulate the normalised weights over g (fixed order g = 0..gn-1)
+        __syncthreads();
         for (int j = tid; j < p.N; j += kThreads) {
             double a = acc[j];
             for (int g = 0; g < gn; ++g)
@@ -120,9 +132,9 @@ __global__ void __launch_bounds__(kThreads) score_partial_kernel(ScoreParams p) 
     for (int j = tid; j < p.N; j += kThreads) p.partial[(int64_t)bh * p.N + j] = acc[j];
 }
 
-__global__ void __launch_bounds__(kThreads) score_reduce_kernel(ScoreParams p) {
+__global__ void __launch_bounds__(256) score_reduce_kernel(ScoreParams p) {
     const int b = blockIdx.y;
-    const int j = blockIdx.x * kThreads + threadIdx.x;
+    const int j = blockIdx.x * 256 + threadIdx.x;
     if (j >= p.N) return;
     double a = 0.0;
     for (int h = 0; h < p.H; ++h) a += p.partial[((int64_t)b * p.H + h) * p.N + j];
@@ -153,15 +165,14 @@ cudaError_t launch_partial_d(const ScoreParams &p, cudaStream_t s) {
 }  // namespace
 
 size_t score_smem_bytes(int N, int d) {
-    return sizeof(double) * N + sizeof(float) * (GC * N + GC * d) + sizeof(double) * kThreads +
-           sizeof(float) * 2 * GC;
+    return sizeof(double) * N + sizeof(float) * (GCH * N + GCH * d + 2 * GCH);
 }
 
 cudaError_t launch_score(const ScoreParams &p, cudaStream_t s) {
     cudaError_t e = p.bf16 ? launch_partial_d<bf16>(p, s) : launch_partial_d<float>(p, s);
     if (e != cudaSuccess) return e;
-    dim3 grid((p.N + kThreads - 1) / kThreads, p.B);
-    score_reduce_kernel<<<grid, kThreads, 0, s>>>(p);
+    dim3 grid((p.N + 255) / 256, p.B);
+    score_reduce_kernel<<<grid, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -192,3 +192,15 @@ MAR_DEVINL bool elect_one() {
 
 }  // namespace tc5
 }  // namespace mar
+
+namespace mar {
+namespace tc5 {
+MAR_DEVINL void tma_load_2d(void *dst, const CUtensorMap *m, int c0, int c1, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];\n" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+}  // namespace tc5
+}  // namespace mar

@@ -5,20 +5,22 @@
 // they form the active set. Candidates exclude the generating and just-decoded tokens.
 //
 // One CTA per batch row. Scores map to 32-bit keys that order like the floats
-// (sign-magnitude flip); a 4-pass MSB-first radix select over those keys finds the
-// K-th largest value T and how many of the candidates equal to T are taken. Equal
-// scores go to the lower position: candidates with key > T are all selected, and the
-// first `take` candidates with key == T in position order. Selected positions are
-// written in ascending order by a block-wide prefix sum, so the result is exact and
-// deterministic.
+// (sign-magnitude flip), so the selection is exact on the fp32 values. A candidate j is
+// selected when fewer than K candidates precede it in the order (key desc, position
+// asc). For N <= kRankN each thread counts that rank directly against all candidates
+// in shared memory (one pass, broadcast reads). Larger rows use a 4-pass MSB-first radix
+// select over the keys, which finds the K-th largest value T and how many candidates
+// equal to T are taken (the lowest positions first). Selected positions are written in
+// ascending order by a block-wide prefix sum, so the result is deterministic.
 #include "common.cuh"
 #include "score.h"
 
 namespace mar {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int kMaxN = 8192;
+constexpr int kRankN = 1152;
 
 MAR_DEVINL uint32_t order_key(float f) {
     uint32_t u = __float_as_uint(f);
@@ -73,6 +75,31 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkParams p) {
         cand[pos] = 0;
     }
     if (p.K == 0) return;
+    if (N <= kRankN) {
+        __syncthreads();
+        int base = 0;
+        for (int j0 = 0; j0 < N; j0 += kThreads) {
+            const int j = j0 + tid;
+            bool sel = false;
+            if (j < N && cand[j]) {
+                const uint32_t kj = keys[j];
+                int rank = 0;
+                for (int i = 0; i < N; ++i) {
+                    const uint32_t ki = keys[i];
+                    rank += (cand[i] && (ki > kj || (ki == kj && i < j))) ? 1 : 0;
+                }
+                sel = rank < p.K;
+            }
+            int tot;
+            const int slot = base + block_excl_scan(sel ? 1 : 0, warp_sums, &tot);
+            base += tot;
+            if (sel && slot < p.K) {
+                if (p.out) p.out[(int64_t)b * p.K + slot] = j;
+                if (p.active) p.active[(int64_t)b * (p.E + p.K) + p.E + slot] = j;
+            }
+        }
+        return;
+    }
     if (tid == 0) {
         sel_prefix = 0u;
         sel_remaining = p.K;
