@@ -89,7 +89,7 @@ int mar_attn_full(const mar_shape *s, const void *Q, const void *K, const void *
     p.B = s->B; p.H = s->H; p.N = s->N; p.d = s->d;
     p.nq = s->N; p.n_dense = s->N; p.A = 0; p.fuse_scatter = 0;
     p.scale = resolve_scale(scale, s->d);
-    cudaError_t e = (s->dtype == MAR_BF16) ? mar::launch_attn_bf16_mma(p, st) : mar::launch_attn_f32(p, st);
+    cudaError_t e = (s->dtype == MAR_BF16) ? mar::launch_attn_bf16(p, st) : mar::launch_attn_f32(p, st);
     if (e != cudaSuccess) return cuda_fail(e);
 
     if (want_score) {
@@ -135,7 +135,7 @@ int mar_attn_cache_aware(const mar_shape *s, int32_t A, const void *Q_A, const v
     p.B = s->B; p.H = s->H; p.N = s->N; p.d = s->d;
     p.nq = A; p.n_dense = A; p.A = A; p.fuse_scatter = fuse_scatter ? 1 : 0;
     p.scale = resolve_scale(scale, s->d);
-    cudaError_t e = (s->dtype == MAR_BF16) ? mar::launch_attn_bf16_mma(p, st) : mar::launch_attn_f32(p, st);
+    cudaError_t e = (s->dtype == MAR_BF16) ? mar::launch_attn_bf16(p, st) : mar::launch_attn_f32(p, st);
     if (e != cudaSuccess) return cuda_fail(e);
     return MAR_OK;
 }
@@ -186,7 +186,7 @@ int mar_refresh_topk(int32_t B, int32_t N, const float *score, const int32_t *ex
                      int32_t K, int32_t *out_idx, int32_t *active_out, uint32_t *d_status,
                      mar_stream_t stream) {
     if (B < 0 || N < 0 || E < 0 || K < 0) return MAR_ERR_ARG;
-    if (N > 8192) return MAR_ERR_SHAPE;
+    if (N > 4096) return MAR_ERR_SHAPE;
     if (E > N || K > N - E) return MAR_ERR_ARG;
     if (B == 0 || N == 0) return MAR_OK;
     if (!score || (E > 0 && !exclude_idx)) return MAR_ERR_ARG;

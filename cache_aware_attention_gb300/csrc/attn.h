@@ -32,5 +32,13 @@ struct AttnParams {
 // Launchers. Return the cudaError_t of the launch.
 cudaError_t launch_attn_f32(const AttnParams &p, cudaStream_t s);
 cudaError_t launch_attn_bf16_mma(const AttnParams &p, cudaStream_t s);
+// tcgen05/TMEM/TMA kernel (head dim 64).
+bool attn_tc5_supported(const AttnParams &p);
+cudaError_t launch_attn_bf16_tc5(const AttnParams &p, cudaStream_t s);
+
+// bf16 attention: the tcgen05 kernel where it supports the shape, else the mma.sync one.
+inline cudaError_t launch_attn_bf16(const AttnParams &p, cudaStream_t s) {
+    return attn_tc5_supported(p) ? launch_attn_bf16_tc5(p, s) : launch_attn_bf16_mma(p, s);
+}
 
 }  // namespace mar

@@ -69,34 +69,53 @@ __global__ void __launch_bounds__(kThreads) score_partial_kernel(ScoreParams p) 
             qs[t] = v;
         }
         __syncthreads();
-        // logits: one key row per thread, all generating queries of the pass
+        // logits: one key row per thread, all generating queries of the pass. The key row
+        // is held in registers 32 columns at a time; query rows are read from shared
+        // memory as float4 broadcasts. Accumulation runs over c in ascending order.
         for (int j = tid; j < p.N; j += kThreads) {
             float dot[GCH];
 #pragma unroll
             for (int g = 0; g < GCH; ++g) dot[g] = 0.f;
             const T *kr = Kbh + (int64_t)j * D;
-#pragma unroll 2
-            for (int c0 = 0; c0 < D; c0 += 8) {
-                float kv[8];
-                if constexpr (sizeof(T) == 2) {
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(kr + c0);
-                    const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = __bfloat1622float2(h2[e]);
-                        kv[2 * e] = f.x;
-                        kv[2 * e + 1] = f.y;
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float kv[32];
+                const int w = (D - c0) < 32 ? (D - c0) : 32;   // 32, or 16 for the tail of d=80
+#pragma unroll
+                for (int e8 = 0; e8 < 4; ++e8) {
+                    if (8 * e8 < w) {
+                        if constexpr (sizeof(T) == 2) {
+                            const uint4 raw = *reinterpret_cast<const uint4 *>(kr + c0 + 8 * e8);
+                            const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = __bfloat1622float2(h2[e]);
+                                kv[8 * e8 + 2 * e] = f.x;
+                                kv[8 * e8 + 2 * e + 1] = f.y;
+                            }
+                        } else {
+                            const float4 a = *reinterpret_cast<const float4 *>(kr + c0 + 8 * e8);
+                            const float4 bq = *reinterpret_cast<const float4 *>(kr + c0 + 8 * e8 + 4);
+                            kv[8 * e8 + 0] = a.x; kv[8 * e8 + 1] = a.y; kv[8 * e8 + 2] = a.z; kv[8 * e8 + 3] = a.w;
+                            kv[8 * e8 + 4] = bq.x; kv[8 * e8 + 5] = bq.y; kv[8 * e8 + 6] = bq.z; kv[8 * e8 + 7] = bq.w;
+                        }
                     }
-                } else {
-                    const float4 a = *reinterpret_cast<const float4 *>(kr + c0);
-                    const float4 bq = *reinterpret_cast<const float4 *>(kr + c0 + 4);
-                    kv[0] = a.x; kv[1] = a.y; kv[2] = a.z; kv[3] = a.w;
-                    kv[4] = bq.x; kv[5] = bq.y; kv[6] = bq.z; kv[7] = bq.w;
                 }
 #pragma unroll
                 for (int g = 0; g < GCH; ++g) {
+                    if (g < gn) {
+                        const float4 *q4 = reinterpret_cast<const float4 *>(qs + g * D + c0);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) dot[g] = fmaf(qs[g * D + c0 + e], kv[e], dot[g]);
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            if (4 * e4 < w) {
+                                const float4 q = q4[e4];
+                                dot[g] = fmaf(q.x, kv[4 * e4 + 0], dot[g]);
+                                dot[g] = fmaf(q.y, kv[4 * e4 + 1], dot[g]);
+                                dot[g] = fmaf(q.z, kv[4 * e4 + 2], dot[g]);
+                                dot[g] = fmaf(q.w, kv[4 * e4 + 3], dot[g]);
+                            }
+                        }
+                    }
                 }
             }
 #pragma unroll

@@ -16,7 +16,7 @@
 namespace mar {
 namespace tc5 {
 
-constexpr uint32_t kSpinLimit = 1u << 24;  // polls before a wait gives up (~ seconds)
+constexpr uint32_t kSpinLimit = 1u << 20;  // polls before a wait gives up (about a second)
 
 // ------------------------------------------------------------------------ mbarrier
 MAR_DEVINL void mbar_init(uint64_t *bar, uint32_t count) {

@@ -18,8 +18,8 @@
 namespace mar {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kMaxN = 8192;
+constexpr int kThreads = 1024;
+constexpr int kMaxN = 4096;
 constexpr int kRankN = 1152;
 
 MAR_DEVINL uint32_t order_key(float f) {
@@ -53,6 +53,7 @@ MAR_DEVINL int block_excl_scan(int v, int *warp_sums, int *total) {
 __global__ void __launch_bounds__(kThreads) topk_kernel(TopkParams p) {
     __shared__ uint32_t keys[kMaxN];
     __shared__ unsigned char cand[kMaxN];
+    __shared__ uint64_t wide[kRankN];
     __shared__ int hist[256];
     __shared__ int warp_sums[kThreads / 32];
     __shared__ uint32_t sel_prefix;
@@ -76,18 +77,19 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkParams p) {
     }
     if (p.K == 0) return;
     if (N <= kRankN) {
+        // rank = number of candidates before j in (key desc, position asc) order; one
+        // 64-bit compare per candidate (non-candidates map to 0 and never precede).
+        for (int j = tid; j < N; j += kThreads)
+            wide[j] = cand[j] ? (((uint64_t)keys[j] << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)j)) : 0ull;
         __syncthreads();
         int base = 0;
         for (int j0 = 0; j0 < N; j0 += kThreads) {
             const int j = j0 + tid;
             bool sel = false;
             if (j < N && cand[j]) {
-                const uint32_t kj = keys[j];
+                const uint64_t kj = wide[j];
                 int rank = 0;
-                for (int i = 0; i < N; ++i) {
-                    const uint32_t ki = keys[i];
-                    rank += (cand[i] && (ki > kj || (ki == kj && i < j))) ? 1 : 0;
-                }
+                for (int i = 0; i < N; ++i) rank += (wide[i] > kj) ? 1 : 0;
                 sel = rank < p.K;
             }
             int tot;

@@ -180,7 +180,7 @@ int mar_kv_gather(const mar_shape *shape, int32_t A, int32_t n_tensors,
  *  out_idx      [B,K] int32: the chosen positions in ascending order (or NULL).
  *  active_out   [B,E+K] int32: exclude_idx[b] followed by out_idx[b] -- the
  *               active set [generating, just-decoded, refreshing] (or NULL).
- * Errors: K > N - E returns MAR_ERR_ARG. Limits: N <= 8192.
+ * Errors: K > N - E returns MAR_ERR_ARG. Limits: N <= 4096 (MAR_ERR_SHAPE beyond).
  */
 int mar_refresh_topk(int32_t B, int32_t N, const float *score, const int32_t *exclude_idx,
                      int32_t E, int32_t K, int32_t *out_idx, int32_t *active_out,

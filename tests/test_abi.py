@@ -91,7 +91,7 @@ def test_cache_aware_validation(lib):
 def test_topk_and_cfg_validation(lib):
     P = ctypes.c_void_p
     assert lib.mar_refresh_topk(2, 10, P(FAKE), P(FAKE), 4, 7, P(FAKE), None, None, None) == -1  # K > N-E
-    assert lib.mar_refresh_topk(2, 9000, P(FAKE), P(FAKE), 4, 7, P(FAKE), None, None, None) == -2
+    assert lib.mar_refresh_topk(2, 5000, P(FAKE), P(FAKE), 4, 7, P(FAKE), None, None, None) == -2
     assert lib.mar_refresh_topk(2, 10, P(FAKE), P(FAKE), 4, 3, None, None, None, None) == -1  # no output
     assert lib.mar_refresh_topk(2, 10, P(FAKE), P(FAKE), 4, 0, None, None, None, None) == 0   # K = 0
     assert lib.mar_cfg_residual(5, 10, P(FAKE), P(FAKE), P(FAKE), ctypes.c_float(0), None, None) == -1

@@ -284,7 +284,7 @@ def test_score_and_topk(name, G, K):
 
 
 @pytest.mark.parametrize("N,E,K,levels", [(320, 8, 32, 0), (320, 8, 32, 5), (1088, 50, 64, 3), (64, 4, 4, 0),
-                                          (300, 0, 300, 2), (5000, 10, 700, 0), (20, 3, 0, 0)])
+                                          (300, 0, 300, 2), (4000, 10, 700, 0), (20, 3, 0, 0)])
 def test_topk_selection_bit_exact(N, E, K, levels):
     g = np.random.default_rng(N + K)
     B = 6
