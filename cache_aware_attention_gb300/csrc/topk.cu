@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkParams p) {
     if (N <= kRankN) {
         // rank = number of candidates before j in (key desc, position asc) order; one
         // 64-bit compare per candidate (non-candidates map to 0 and never precede).
+        __syncthreads();  // exclusion flags written above
         for (int j = tid; j < N; j += kThreads)
             wide[j] = cand[j] ? (((uint64_t)keys[j] << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)j)) : 0ull;
         __syncthreads();
