@@ -264,17 +264,9 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc5_kernel(const __grid_cons
             tc_fence_after();
             if (live) {
                 float v[64];
-                {
-                    float a[32], c[32];
-                    tmem_ld32(lane_addr(tmS0, warp, 64 * buf), a);
-                    tmem_ld32(lane_addr(tmS0, warp, 64 * buf + 32), c);
-                    tmem_wait_ld();
+                tmem_ld64(lane_addr(tmS0, warp, 64 * buf), v);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        v[i] = a[i] * sl2;
-                        v[32 + i] = c[i] * sl2;
-                    }
-                }
+                for (int i = 0; i < 64; ++i) v[i] *= sl2;
                 // mask slots that are not keys: past the list, or the gather4 padding
                 const int s0 = j * BN;
                 const bool all_valid = P.gather ? (s0 + BN <= n_slots && (s0 >= dense_slots || s0 + BN <= p.A))
@@ -309,7 +301,6 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc5_kernel(const __grid_cons
                         for (int c0 = 0; c0 < D; c0 += 16) {
                             float o[16];
                             tmem_ld16(lane_addr(tmO, warp, c0), o);
-                            tmem_wait_ld();
                             uint32_t w[16];
 #pragma unroll
                             for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(o[i] * factor);
@@ -352,7 +343,6 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc5_kernel(const __grid_cons
             for (int c0 = 0; c0 < D; c0 += 16) {
                 float o[16];
                 tmem_ld16(lane_addr(tmO, warp, c0), o);
-                tmem_wait_ld();
                 if (row < p.nq) {
                     uint4 u0, u1;
                     u0.x = pack_bf16x2(o[0] * inv, o[1] * inv);
