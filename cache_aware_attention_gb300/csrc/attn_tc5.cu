@@ -334,6 +334,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc5_kernel(const __grid_cons
             if (lane == 0) mbar_arrive(&bars[P_FULL + buf]);
             if (!ok) break;
         }
+        // A parity wait is only unambiguous when the phase before it is known complete:
+        // the S of the last block was issued after PV of block nblk-3, so wait for PV of
+        // block nblk-2 first, then for the last one.
+        if (ok && nblk >= 2) ok = mbar_wait(&bars[O_DONE], (nblk - 2) & 1, p.status, abort_flag);
         if (ok && mbar_wait(&bars[O_DONE], (nblk - 1) & 1, p.status, abort_flag) && live) {
             tc_fence_after();
             const int row = q0 + tid;
