@@ -19,6 +19,7 @@ from . import _build
 
 __all__ = [
     "MarError", "MarShape", "load", "library_path", "mar_attn_full", "mar_attn_full_workspace_bytes",
+    "mar_attn_full_noalloc",
     "mar_attn_cache_aware", "mar_kv_scatter", "mar_kv_gather", "mar_refresh_topk",
     "mar_cfg_residual", "mar_status_read", "mar_error_string", "mar_version",
     "MAR_F32", "MAR_BF16", "MAR_CFG_APPLY", "MAR_CFG_UPDATE",
@@ -74,6 +75,8 @@ def load(path: str | None = None):
         "mar_refresh_topk": ([I32, I32, P, P, I32, I32, P, P, P, P], ctypes.c_int),
         "mar_cfg_residual": ([I32, I64, P, P, P, F, P, P], ctypes.c_int),
         "mar_status_read": ([P, P, P], ctypes.c_int),
+        "mar_noalloc_scratch_bytes": ([], SZ),
+        "mar_attn_full_noalloc": ([SP, P, P, P, P, F, P, I32, P, P, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -150,6 +153,23 @@ def mar_attn_full(Q, K, V, O=None, scale: float = 0.0, gen_idx=None, score_out=N
                            _ptr(gen_idx), G, _ptr(score_out), _ptr(lse_out), _ptr(workspace), wb,
                            _ptr(status), _stream(stream))
     _check("mar_attn_full", rc)
+    return O
+
+
+def mar_attn_full_noalloc(Q, K, V, O=None, scale: float = 0.0, gen_idx=None, score_out=None,
+                          lse_out=None, status=None, stream=None):
+    """mar_attn_full without a workspace argument: the score's scratch is the library's
+    built-in buffer, so the call allocates no device memory of its own (for callers that
+    must not allocate). Overlapping calls on one device race on that buffer."""
+    lib = load()
+    s = _shape(Q)
+    if O is None:
+        O = torch.empty_like(Q)
+    G = 0 if gen_idx is None else int(gen_idx.shape[1])
+    rc = lib.mar_attn_full_noalloc(ctypes.byref(s), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), float(scale),
+                                   _ptr(gen_idx), G, _ptr(score_out), _ptr(lse_out), _ptr(status),
+                                   _stream(stream))
+    _check("mar_attn_full_noalloc", rc)
     return O
 
 

@@ -40,6 +40,11 @@ float resolve_scale(float scale, int d) { return scale > 0.f ? scale : 1.0f / st
 
 }  // namespace
 
+namespace mar {
+// Lets other translation units of the library report a failed CUDA call.
+int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+}  // namespace mar
+
 extern "C" {
 
 const char *mar_error_string(int code) {
@@ -52,6 +57,8 @@ const char *mar_error_string(int code) {
         case MAR_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
         case MAR_ERR_CUDA: return "CUDA error (see mar_last_cuda_error)";
         case MAR_ERR_NODEV: return "no usable CUDA device";
+        case MAR_ERR_SCRATCH_LIMIT:
+            return "shape needs more scratch than the library's built-in no-allocation buffer holds";
         default: return "unknown error";
     }
 }

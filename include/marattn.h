@@ -18,7 +18,9 @@
  * Conventions shared by every call
  * --------------------------------
  *  - Pointers are caller-owned DEVICE pointers unless stated otherwise. The
- *    library never allocates device memory and keeps no state between calls.
+ *    library allocates no device memory at run time and keeps no state between
+ *    calls, except the fixed scratch buffer of mar_attn_full_noalloc (a static
+ *    device array, see that call).
  *  - Tensors are dense and contiguous in the layouts given below:
  *      Q, K, V, O, cache           [B, H, N, d]   (token rows of d elements)
  *      Q_A, K_A, V_A, O_A          [B, H, A, d]   (active rows, in idx order)
@@ -61,7 +63,8 @@ enum mar_result {
     MAR_ERR_ALIGN = -4,     /* pointer not 16-byte aligned */
     MAR_ERR_WORKSPACE = -5, /* workspace NULL, too small or misaligned */
     MAR_ERR_CUDA = -6,      /* a CUDA call failed; see mar_last_cuda_error() */
-    MAR_ERR_NODEV = -7      /* no usable sm_103 device */
+    MAR_ERR_NODEV = -7,     /* no usable sm_103 device */
+    MAR_ERR_SCRATCH_LIMIT = -8 /* needs more scratch than the built-in no-allocation buffer */
 };
 
 /* Bits OR-ed into *d_status by the kernels. */
@@ -113,6 +116,31 @@ int mar_attn_full(const mar_shape *shape, const void *Q, const void *K, const vo
                   void *O, float scale, const int32_t *gen_idx, int32_t G,
                   float *score_out, float *lse_out, void *workspace,
                   size_t workspace_bytes, uint32_t *d_status, mar_stream_t stream);
+
+/*
+ * mar_attn_full_noalloc -- mar_attn_full for callers that cannot allocate.
+ *
+ * The paper has no counterpart to this call; it exists for callers that must not
+ * allocate device memory, such as plugins inside a host framework whose allocator
+ * owns the device pool, or decode loops that cannot risk an allocation stalling or
+ * failing mid-step. It computes exactly what mar_attn_full computes, with the same
+ * arguments except the workspace: the score's scratch lives in a buffer compiled into
+ * the library (mar_noalloc_scratch_bytes() bytes, 24 MiB, held on every GPU that loads
+ * the library until the process exits).
+ *  - Returns MAR_ERR_SCRATCH_LIMIT when mar_attn_full_workspace_bytes() of the shape
+ *    exceeds that buffer (B*H*N above 3,145,728 with a score requested).
+ *  - Allocates nothing. The first call made on a device looks up the buffer's device
+ *    address; make that first call before any stream capture.
+ *  - All calls share the one buffer: calls that can overlap on the GPU (different
+ *    streams, or different host threads on one device) race and must be serialised
+ *    by the caller. The buffer keeps the previous call's contents; nothing in it needs
+ *    to start at zero.
+ */
+size_t mar_noalloc_scratch_bytes(void);
+int mar_attn_full_noalloc(const mar_shape *shape, const void *Q, const void *K, const void *V,
+                          void *O, float scale, const int32_t *gen_idx, int32_t G,
+                          float *score_out, float *lse_out, uint32_t *d_status,
+                          mar_stream_t stream);
 
 /*
  * mar_attn_cache_aware -- split attention of the active queries over fresh

@@ -47,7 +47,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_version_and_error_strings(lib):
     assert mar.mar_version() >= 10000
-    for code in range(0, -8, -1):
+    for code in range(0, -9, -1):
         assert mar.mar_error_string(code)
 
 
