@@ -7,10 +7,13 @@
 // MARché notes, Key Design 2: each active query attends over fresh K_A/V_A and stored
 // cached K/V as two partial softmax sums merged by the safe online-softmax rule (running
 // max, running sum), with no concatenated key buffer in memory. The key list is streamed
-// in blocks of 64 slots straight from the two sources into shared memory: TMA tile loads
-// for contiguous rows (full attention), TMA gather4 loads (four rows per instruction) of
-// the active rows and of the cached rows named by an in-CTA list built from the active
-// indices (cache rows of active positions are never read).
+// in blocks of 64 rows straight from the two sources into shared memory with TMA tile
+// loads: first the fresh active rows (cache-aware) or all rows (full attention), then,
+// for cache-aware attention, the cache slab of the (b, h) in position order. Cache rows
+// of active positions hold stale values: they are masked out of the softmax by a bitmap
+// of the active positions built in the CTA, so they never contribute (they are read,
+// costing A/N extra bytes, because one tile load per 64 rows runs at the TMA unit's
+// full rate while a per-row gather is bound by its request rate).
 //
 // CTA = one (b, h) and 128 query rows; 6 warps:
 //   warps 0-3  softmax + epilogue; thread t owns query row t (tensor-memory lane t)
@@ -18,6 +21,8 @@
 //   warp 5     MMA issuer (one lane):  S_j = Q K_j^T  (M=128, N=64, K=d, K-major operands)
 //                                       O  += P_j V_j  (M=128, N=d, K=64, P from TMEM,
 //                                                       V MN-major)
+//              It polls its barriers and issues whichever MMA is ready: PV_j as soon as
+//              P_j is written, S_{j+2} as soon as PV_j has released its buffer.
 // Tensor memory (256 columns): two S buffers of 64 columns (S_j, S_{j+1}), each
 // overwritten in place by P_j as packed bf16 pairs, and O (d columns) accumulated by the
 // MMAs across all blocks. While the softmax warps turn S_j into P_j, the tensor core
@@ -64,14 +69,14 @@ struct Cfg {
     static constexpr uint32_t sKa = 0, sVa = kKa, sKb = 2 * kKa, sVb = 2 * kKa + kKb;
 };
 
-enum Bar { Q_FULL = 0, S_FULL = 1, P_FULL = 3, O_DONE = 5, KV_FULL = 6 };  // then KV_EMPTY
+enum Bar { Q_FULL = 0, S_FULL = 1, P_FULL = 3, O_DONE = 5, KV_FULL = 7 };  // then KV_EMPTY
 
 template <int D>
 struct Tc5Params {
     CUtensorMap mQa, mQb;    // 3-D [BH, nq, D]: box {64,128,1} (SW128) / {16,128,1} (SW32)
-    CUtensorMap mKa, mKb;    // full: 3-D [BH, n_dense, D] box {64|16, 64, 1};
-    CUtensorMap mVa, mVb;    // cache-aware: 2-D [BH*A, D] box {64|16, 1}
-    CUtensorMap mKca, mKcb;  // cache-aware: 2-D [BH*N, D] box {64|16, 1}
+    CUtensorMap mKa, mKb;    // 3-D [BH, n_dense, D], box {64|16, 64, 1}: all rows / active rows
+    CUtensorMap mVa, mVb;
+    CUtensorMap mKca, mKcb;  // cache-aware: 3-D [BH, N, D], box {64|16, 64, 1}
     CUtensorMap mVca, mVcb;
     AttnParams a;
     int gather;
@@ -93,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc5_kernel(const __grid_cons
     uint64_t *kv_empty = bars + KV_FULL + S;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + KV_FULL + 2 * S);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    int32_t *sList = reinterpret_cast<int32_t *>(tmem_slot + 4);
+    uint32_t *bitmap = reinterpret_cast<uint32_t *>(tmem_slot + 4);  // active positions
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nqt = (p.nq + BM - 1) / BM;
@@ -109,6 +114,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc5_kernel(const __grid_cons
             mbar_init(&bars[P_FULL + i], 4);
         }
         mbar_init(&bars[O_DONE], 1);
+        mbar_init(&bars[O_DONE + 1], 1);
         for (int i = 0; i < S; ++i) {
             mbar_init(&bars[KV_FULL + i], 1);
             mbar_init(&kv_empty[i], 1);
@@ -124,62 +130,53 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc5_kernel(const __grid_cons
         tma_load_3d(sm + C::oQa, &P.mQa, 0, q0, bh, &bars[Q_FULL]);
         if constexpr (C::DB > 0) tma_load_3d(sm + C::oQb, &P.mQb, 64, q0, bh, &bars[Q_FULL]);
     }
-    int Ccnt = 0;
     if (P.gather) {
-        uint32_t *bitmap = reinterpret_cast<uint32_t *>(sList + p.N);
-        int32_t *wt = reinterpret_cast<int32_t *>(bitmap + ((p.N + 31) >> 5));
-        Ccnt = build_cached_list(p.idx + (int64_t)b * p.A, p.A, p.N, bitmap, sList, wt, p.status);
-    } else {
+        // bitmap of the active positions of row b (their cache rows are stale)
+        const int words = 2 * ((p.N + BN - 1) / BN);
+        for (int w = tid; w < words; w += kThreads) bitmap[w] = 0u;
         __syncthreads();
+        uint32_t bad = 0;
+        for (int a = tid; a < p.A; a += kThreads) {
+            const int pos = p.idx[(int64_t)b * p.A + a];
+            if (pos < 0 || pos >= p.N) {
+                bad |= MAR_STATUS_INDEX_RANGE;
+                continue;
+            }
+            const uint32_t old = atomicOr(&bitmap[pos >> 5], 1u << (pos & 31));
+            if (old & (1u << (pos & 31))) bad |= MAR_STATUS_INDEX_DUP;
+        }
+        if (bad) report(p.status, bad);
     }
+    __syncthreads();
     const uint32_t tm = *tmem_slot;
     const uint32_t tmS0 = tm, tmO = tm + 128;
 
-    const int dense_slots = P.gather ? ((p.A + 3) & ~3) : p.n_dense;
-    const int n_slots = P.gather ? dense_slots + Ccnt : p.n_dense;
-    const int nblk = (n_slots + BN - 1) / BN;
+    // key blocks: nd blocks of dense rows (the fresh active rows, or all rows of K/V), then
+    // for cache-aware attention nc blocks of the cache slab in position order
+    const int nd = (p.n_dense + BN - 1) / BN;
+    const int nc = (P.gather && p.A < p.N) ? (p.N + BN - 1) / BN : 0;
+    const int nblk = nd + nc;
 
     if (warp == 4) {
         // ------------------------------------------------------------ producer
-        for (int j = 0; j < nblk; ++j) {
-            const int st = j % S;
-            if (!mbar_wait(&kv_empty[st], ((j / S) & 1) ^ 1, p.status, abort_flag)) break;
-            unsigned char *stg = sm + C::oStage + st * C::kStageBytes;
-            if (lane == 0) mbar_arrive_expect_tx(&bars[KV_FULL + st], C::kKV);
-            __syncwarp();
-            if (!P.gather) {
-                if (lane == 0) {
-                    tma_load_3d(stg + C::sKa, &P.mKa, 0, j * BN, bh, &bars[KV_FULL + st]);
-                    tma_load_3d(stg + C::sVa, &P.mVa, 0, j * BN, bh, &bars[KV_FULL + st]);
-                    if constexpr (C::DB > 0) {
-                        tma_load_3d(stg + C::sKb, &P.mKb, 64, j * BN, bh, &bars[KV_FULL + st]);
-                        tma_load_3d(stg + C::sVb, &P.mVb, 64, j * BN, bh, &bars[KV_FULL + st]);
-                    }
-                }
-            } else {
-                // lane l: group g = l & 15 (slots 4g..4g+3 of the block); lanes 0-15 -> K, 16-31 -> V
-                const int g = lane & 15;
-                const bool isV = lane >= 16;
-                const int s0 = j * BN + 4 * g;
-                int r[4];
-                const bool dense = (s0 < dense_slots) || (Ccnt == 0);
-                if (dense) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) r[i] = bh * p.A + min(s0 + i, p.A - 1);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) r[i] = bh * p.N + sList[min(s0 + i - dense_slots, Ccnt - 1)];
-                }
-                const CUtensorMap *ma = dense ? (isV ? &P.mVa : &P.mKa) : (isV ? &P.mVca : &P.mKca);
-                tma_gather4(stg + (isV ? C::sVa : C::sKa) + 512 * g, ma, 0, r[0], r[1], r[2], r[3],
-                            &bars[KV_FULL + st]);
+        if (lane == 0) {
+            for (int j = 0; j < nblk; ++j) {
+                const int st = j % S;
+                if (!mbar_wait(&kv_empty[st], ((j / S) & 1) ^ 1, p.status, abort_flag)) break;
+                unsigned char *stg = sm + C::oStage + st * C::kStageBytes;
+                uint64_t *fb = &bars[KV_FULL + st];
+                mbar_arrive_expect_tx(fb, C::kKV);
+                const bool dense = j < nd;
+                const int row = (dense ? j : j - nd) * BN;
+                tma_load_3d(stg + C::sKa, dense ? &P.mKa : &P.mKca, 0, row, bh, fb);
+                tma_load_3d(stg + C::sVa, dense ? &P.mVa : &P.mVca, 0, row, bh, fb);
                 if constexpr (C::DB > 0) {
-                    const CUtensorMap *mb = dense ? (isV ? &P.mVb : &P.mKb) : (isV ? &P.mVcb : &P.mKcb);
-                    tma_gather4(stg + (isV ? C::sVb : C::sKb) + 128 * g, mb, 64, r[0], r[1], r[2], r[3],
-                                &bars[KV_FULL + st]);
+                    tma_load_3d(stg + C::sKb, dense ? &P.mKb : &P.mKcb, 64, row, bh, fb);
+                    tma_load_3d(stg + C::sVb, dense ? &P.mVb : &P.mVcb, 64, row, bh, fb);
                 }
             }
         }
+        __syncwarp();
     } else if (warp == 5) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -188,47 +185,61 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc5_kernel(const __grid_cons
             const uint32_t idOb = idesc_bf16(BM, 16, 0, 1);
             const uint64_t dQa = smem_desc(sm + C::oQa, 16, 1024, Swz::B128);
             const uint64_t dQb = smem_desc(sm + C::oQb, 16, 256, Swz::B32);
-            auto issue_S = [&](int j) {
-                const int st = j % S;
-                const unsigned char *stg = sm + C::oStage + st * C::kStageBytes;
-                const uint64_t dKa = smem_desc(stg + C::sKa, 16, 1024, Swz::B128);
-                const uint32_t dst = tmS0 + 64 * (j & 1);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) mma_ss(dst, desc_advance(dQa, 32 * k), desc_advance(dKa, 32 * k), idS, k > 0);
-                if constexpr (C::DB > 0) mma_ss(dst, dQb, smem_desc(stg + C::sKb, 16, 256, Swz::B32), idS, 1);
-                mma_commit(&bars[S_FULL + (j & 1)]);
-            };
             bool ok = mbar_wait(&bars[Q_FULL], 0, p.status, abort_flag);
-            for (int j = 0; ok && j < 2 && j < nblk; ++j) {
-                ok = mbar_wait(&bars[KV_FULL + j % S], (j / S) & 1, p.status, abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                issue_S(j);
-            }
-            for (int j = 0; ok && j < nblk; ++j) {
-                const int st = j % S;
-                ok = mbar_wait(&bars[P_FULL + (j & 1)], (j >> 1) & 1, p.status, abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                const unsigned char *stg = sm + C::oStage + st * C::kStageBytes;
-                const uint64_t dVa = smem_desc(stg + C::sVa, 1024, 1024, Swz::B128);
-                const uint64_t dVb = smem_desc(stg + C::sVb, 256, 256, Swz::B32);
-                const uint32_t pcol = tmS0 + 64 * (j & 1);
+            int next_s = 0, next_pv = 0;
+            uint32_t idle = 0;
+            while (ok && next_pv < nblk) {
+                bool progress = false;
+                // S_j: its K block has landed and PV_{j-2} has released S/P buffer j & 1.
+                // Each barrier is tested one phase at a time, in order, so parities are exact.
+                if (next_s < nblk && next_s < next_pv + 2) {
+                    const int j = next_s;
+                    bool ready = mbar_try_wait(&bars[KV_FULL + j % S], (j / S) & 1);
+                    if (ready && j >= 2) ready = mbar_try_wait(&bars[O_DONE + (j & 1)], ((j - 2) >> 1) & 1);
+                    if (ready) {
+                        tc_fence_after();
+                        const unsigned char *stg = sm + C::oStage + (j % S) * C::kStageBytes;
+                        const uint64_t dKa = smem_desc(stg + C::sKa, 16, 1024, Swz::B128);
+                        const uint32_t dst = tmS0 + 64 * (j & 1);
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k) {
-                    const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
-                    mma_ts(tmO, pcol + 8 * k, desc_advance(dVa, 2048 * k), idOa, acc);
-                    if constexpr (C::DB > 0) mma_ts(tmO + 64, pcol + 8 * k, desc_advance(dVb, 512 * k), idOb, acc);
+                        for (int k = 0; k < 4; ++k)
+                            mma_ss(dst, desc_advance(dQa, 32 * k), desc_advance(dKa, 32 * k), idS, k > 0);
+                        if constexpr (C::DB > 0) mma_ss(dst, dQb, smem_desc(stg + C::sKb, 16, 256, Swz::B32), idS, 1);
+                        mma_commit(&bars[S_FULL + (j & 1)]);
+                        ++next_s;
+                        progress = true;
+                    }
                 }
-                mma_commit(&bars[O_DONE]);
-                mma_commit(&kv_empty[st]);
-                if (j + 2 < nblk) {
-                    // S_{j+2} reuses P_j's columns: wait until PV_j has consumed them
-                    ok = mbar_wait(&bars[O_DONE], j & 1, p.status, abort_flag);
-                    if (ok) ok = mbar_wait(&bars[KV_FULL + (j + 2) % S], ((j + 2) / S) & 1, p.status, abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_S(j + 2);
+                // PV_j: P_j has been written over S_j
+                if (next_pv < next_s) {
+                    const int j = next_pv;
+                    if (mbar_try_wait(&bars[P_FULL + (j & 1)], (j >> 1) & 1)) {
+                        tc_fence_after();
+                        const unsigned char *stg = sm + C::oStage + (j % S) * C::kStageBytes;
+                        const uint64_t dVa = smem_desc(stg + C::sVa, 1024, 1024, Swz::B128);
+                        const uint64_t dVb = smem_desc(stg + C::sVb, 256, 256, Swz::B32);
+                        const uint32_t pcol = tmS0 + 64 * (j & 1);
+#pragma unroll
+                        for (int k = 0; k < BN / 16; ++k) {
+                            const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
+                            mma_ts(tmO, pcol + 8 * k, desc_advance(dVa, 2048 * k), idOa, acc);
+                            if constexpr (C::DB > 0)
+                                mma_ts(tmO + 64, pcol + 8 * k, desc_advance(dVb, 512 * k), idOb, acc);
+                        }
+                        mma_commit(&bars[O_DONE + (j & 1)]);
+                        mma_commit(&kv_empty[j % S]);
+                        ++next_pv;
+                        progress = true;
+                    }
+                }
+                if (progress) {
+                    idle = 0;
+                } else if (*abort_flag) {
+                    ok = false;
+                } else if (++idle > kSpinLimit) {
+                    report(p.status, MAR_STATUS_TIMEOUT_BIT);
+                    *abort_flag = 1;
+                    ok = false;
                 }
             }
         }
@@ -236,7 +247,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc5_kernel(const __grid_cons
     } else {
         // ------------------------------------------------------------ softmax + epilogue
         if (P.gather && p.fuse_scatter && qt == 0) {
-            // Fresh K_A/V_A rows -> cache rows of the active positions (never read here).
+            // Fresh K_A/V_A rows -> cache rows of the active positions. No query of this
+            // launch uses those rows (they are masked as stale), so the order is free.
             const bf16 *Kd = static_cast<const bf16 *>(p.Kd);
             const bf16 *Vd = static_cast<const bf16 *>(p.Vd);
             bf16 *Kc = static_cast<bf16 *>(p.Kc);
@@ -262,26 +274,52 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc5_kernel(const __grid_cons
                 break;
             }
             tc_fence_after();
+            // slots of this block that are keys: dense rows below n_dense; cache rows below
+            // N whose position is not active (active positions hold stale cache rows)
+            uint64_t valid, stale = 0ull;
+            if (j < nd) {
+                const int r = p.n_dense - j * BN;
+                valid = r >= 64 ? ~0ull : ((1ull << r) - 1ull);
+            } else {
+                const int pos0 = (j - nd) * BN;
+                stale = (uint64_t)bitmap[pos0 >> 5] | ((uint64_t)bitmap[(pos0 >> 5) + 1] << 32);
+                valid = ~stale;
+                const int r = p.N - pos0;
+                if (r < 64) {
+                    valid &= (1ull << r) - 1ull;
+                    stale &= (1ull << r) - 1ull;
+                }
+            }
+            if (stale) {
+                // Their P is 0, but 0 x NaN is NaN: clear the stale V rows in shared memory so
+                // that whatever a stale row holds cannot reach O. Whole rows are cleared, so
+                // the swizzle inside a row does not matter.
+                unsigned char *stg = sm + C::oStage + (j % S) * C::kStageBytes;
+                for (int t = tid; t < BN * 8; t += 128)
+                    if ((stale >> (t >> 3)) & 1ull) *reinterpret_cast<uint4 *>(stg + C::sVa + 16 * t) = make_uint4(0, 0, 0, 0);
+                if constexpr (C::DB > 0) {
+                    for (int t = tid; t < BN * 2; t += 128)
+                        if ((stale >> (t >> 1)) & 1ull) *reinterpret_cast<uint4 *>(stg + C::sVb + 16 * t) = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+            }
             if (live) {
                 float v[64];
                 tmem_ld64(lane_addr(tmS0, warp, 64 * buf), v);
-#pragma unroll
-                for (int i = 0; i < 64; ++i) v[i] *= sl2;
-                // mask slots that are not keys: past the list, or the gather4 padding
-                const int s0 = j * BN;
-                const bool all_valid = P.gather ? (s0 + BN <= n_slots && (s0 >= dense_slots || s0 + BN <= p.A))
-                                                : (s0 + BN <= n_slots);
-                if (!all_valid) {
+                float mx = -INFINITY;
+                if (valid == ~0ull) {
 #pragma unroll
                     for (int i = 0; i < 64; ++i) {
-                        const int s = s0 + i;
-                        const bool ok_slot = P.gather ? (s < p.A || (s >= dense_slots && s < n_slots)) : (s < n_slots);
-                        if (!ok_slot) v[i] = -INFINITY;
+                        v[i] *= sl2;
+                        mx = fmaxf(mx, v[i]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) {
+                        v[i] = ((valid >> i) & 1ull) ? v[i] * sl2 : -INFINITY;
+                        mx = fmaxf(mx, v[i]);
                     }
                 }
-                float mx = v[0];
-#pragma unroll
-                for (int i = 1; i < 64; ++i) mx = fmaxf(mx, v[i]);
                 bool rescale = false;
                 float factor = 1.f;
                 if (j == 0) {
@@ -292,8 +330,9 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc5_kernel(const __grid_cons
                     rescale = true;
                 }
                 if (__any_sync(0xffffffffu, rescale)) {
-                    // O holds sum_{i<j} P_i V_i; wait for it and scale rows that raised their max
-                    if (!mbar_wait(&bars[O_DONE], (j - 1) & 1, p.status, abort_flag)) {
+                    // O holds sum_{i<j} P_i V_i; wait for PV_{j-1} and scale the rows that
+                    // raised their max (the other rows use factor 1)
+                    if (!mbar_wait(&bars[O_DONE + ((j - 1) & 1)], ((j - 1) >> 1) & 1, p.status, abort_flag)) {
                         ok = false;
                     } else {
                         tc_fence_after();
@@ -310,21 +349,16 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc5_kernel(const __grid_cons
                     }
                 }
                 float rs = 0.f;
-                uint32_t w[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float p0 = fast_exp2(v[2 * i] - m_use);
-                    const float p1 = fast_exp2(v[2 * i + 1] - m_use);
-                    rs += p0 + p1;
-                    w[i] = pack_bf16x2(p0, p1);
-                }
-                l += rs;
                 uint32_t w0[16], w1[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    w0[i] = w[i];
-                    w1[i] = w[16 + i];
+                    const float p0 = fast_exp2(v[2 * i] - m_use), p1 = fast_exp2(v[2 * i + 1] - m_use);
+                    const float p2 = fast_exp2(v[32 + 2 * i] - m_use), p3 = fast_exp2(v[33 + 2 * i] - m_use);
+                    rs += (p0 + p1) + (p2 + p3);
+                    w0[i] = pack_bf16x2(p0, p1);
+                    w1[i] = pack_bf16x2(p2, p3);
                 }
+                l += rs;
                 tmem_st16(lane_addr(tmS0, warp, 64 * buf), w0);
                 tmem_st16(lane_addr(tmS0, warp, 64 * buf + 16), w1);
                 tmem_wait_st();
@@ -334,11 +368,9 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc5_kernel(const __grid_cons
             if (lane == 0) mbar_arrive(&bars[P_FULL + buf]);
             if (!ok) break;
         }
-        // A parity wait is only unambiguous when the phase before it is known complete:
-        // the S of the last block was issued after PV of block nblk-3, so wait for PV of
-        // block nblk-2 first, then for the last one.
-        if (ok && nblk >= 2) ok = mbar_wait(&bars[O_DONE], (nblk - 2) & 1, p.status, abort_flag);
-        if (ok && mbar_wait(&bars[O_DONE], (nblk - 1) & 1, p.status, abort_flag) && live) {
+        // PV_{nblk-1} was issued after PV_{nblk-3} finished, so its barrier phase is exact;
+        // MMAs complete in order, so its completion covers every earlier PV.
+        if (ok && mbar_wait(&bars[O_DONE + ((nblk - 1) & 1)], ((nblk - 1) >> 1) & 1, p.status, abort_flag) && live) {
             tc_fence_after();
             const int row = q0 + tid;
             const float inv = 1.f / l;
@@ -379,15 +411,6 @@ bool map3(CUtensorMap *m, const void *ptr, int rows, int bh, uint32_t boxw, uint
 }
 
 template <int D>
-bool map_rows(CUtensorMap *m, const void *ptr, int64_t rows, uint32_t boxw) {
-    const uint64_t dims[2] = {(uint64_t)D, (uint64_t)rows};
-    const uint64_t strides[1] = {(uint64_t)D * 2};
-    const uint32_t box[2] = {boxw, 1};
-    return make_map_bf16(m, ptr, 2, dims, strides, box,
-                         boxw == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B);
-}
-
-template <int D>
 cudaError_t launch(const AttnParams &p, cudaStream_t s) {
     using C = Cfg<D>;
     static int configured[64] = {0};
@@ -397,20 +420,17 @@ cudaError_t launch(const AttnParams &p, cudaStream_t s) {
     const int bh = p.B * p.H;
     const uint32_t tw = D == 64 ? 64 : 16;  // tail box width (unused for d = 64)
     bool ok = map3<D>(&P.mQa, p.Q, p.nq, bh, 64, BM) && map3<D>(&P.mQb, p.Q, p.nq, bh, tw, BM);
+    ok = ok && map3<D>(&P.mKa, p.Kd, p.n_dense, bh, 64, BN) && map3<D>(&P.mKb, p.Kd, p.n_dense, bh, tw, BN);
+    ok = ok && map3<D>(&P.mVa, p.Vd, p.n_dense, bh, 64, BN) && map3<D>(&P.mVb, p.Vd, p.n_dense, bh, tw, BN);
     if (P.gather) {
-        const int64_t ra = (int64_t)bh * p.A, rc = (int64_t)bh * p.N;
-        ok = ok && map_rows<D>(&P.mKa, p.Kd, ra, 64) && map_rows<D>(&P.mKb, p.Kd, ra, tw);
-        ok = ok && map_rows<D>(&P.mVa, p.Vd, ra, 64) && map_rows<D>(&P.mVb, p.Vd, ra, tw);
-        ok = ok && map_rows<D>(&P.mKca, p.Kc, rc, 64) && map_rows<D>(&P.mKcb, p.Kc, rc, tw);
-        ok = ok && map_rows<D>(&P.mVca, p.Vc, rc, 64) && map_rows<D>(&P.mVcb, p.Vc, rc, tw);
+        ok = ok && map3<D>(&P.mKca, p.Kc, p.N, bh, 64, BN) && map3<D>(&P.mKcb, p.Kc, p.N, bh, tw, BN);
+        ok = ok && map3<D>(&P.mVca, p.Vc, p.N, bh, 64, BN) && map3<D>(&P.mVcb, p.Vc, p.N, bh, tw, BN);
     } else {
-        ok = ok && map3<D>(&P.mKa, p.Kd, p.n_dense, bh, 64, BN) && map3<D>(&P.mKb, p.Kd, p.n_dense, bh, tw, BN);
-        ok = ok && map3<D>(&P.mVa, p.Vd, p.n_dense, bh, 64, BN) && map3<D>(&P.mVb, p.Vd, p.n_dense, bh, tw, BN);
         P.mKca = P.mKa; P.mKcb = P.mKb; P.mVca = P.mVa; P.mVcb = P.mVb;
     }
     if (!ok) return cudaErrorInvalidValue;
     size_t smem = 1024 + C::oBars + 8 * (KV_FULL + 2 * C::kStages) + 16;
-    if (P.gather) smem += sizeof(int32_t) * (p.N + (p.N + 31) / 32 + kThreads / 32);
+    if (P.gather) smem += sizeof(uint32_t) * 2 * ((p.N + BN - 1) / BN);
     cudaError_t e = ensure_smem(attn_tc5_kernel<D>, smem, configured);
     if (e != cudaSuccess) return e;
     const long long blocks = (long long)((p.nq + BM - 1) / BM) * bh;

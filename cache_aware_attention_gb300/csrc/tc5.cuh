@@ -88,6 +88,9 @@ MAR_DEVINL void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
 MAR_DEVINL void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
 }
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy
+// (tensor core, TMA) accesses.
+MAR_DEVINL void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 MAR_DEVINL void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
 MAR_DEVINL void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
 

@@ -152,8 +152,9 @@ int mar_attn_full_noalloc(const mar_shape *shape, const void *Q, const void *K, 
  *   K_A[b,h,0..A) followed by K_cache[b,h,p,:] for p in C(b)
  * (V likewise) as two partial softmax sums merged by running max and running
  * sum:  z_i = (alpha^(A) V_A + alpha^(C) V_C) / l_i. Cache rows at active
- * positions hold stale values and are never read. The result equals full
- * attention over the concatenated list ([R] Appendix A equivalence).
+ * positions hold stale values and never contribute, whatever they hold (they may
+ * be read and are then masked out). The result equals full attention over the
+ * concatenated list ([R] Appendix A equivalence).
  *
  *  Q_A, K_A, V_A, O_A  [B,H,A,d]; active_idx [B,A] distinct positions in [0,N).
  *  K_cache, V_cache    [B,H,N,d]. Read at cached positions; when fuse_scatter is

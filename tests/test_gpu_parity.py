@@ -200,6 +200,24 @@ def test_cache_aware_px512_sampled_rows():
         P.assert_close(O[sl], O_ref, "bf16", f"512px row {b}")
 
 
+@pytest.mark.parametrize("d", [64, 80])
+def test_cache_aware_stale_rows_never_contribute(d):
+    # Cache rows at active positions are stale; whatever they hold (here NaN and huge
+    # values) must not reach the output.
+    B, H, N, A = 3, 4, 320, 40
+    idx = _active(B, A, N, 81 + d)
+    Q_A, K_A, V_A = (_rand((B, H, A, d), 82 + i, torch.bfloat16) for i in range(3))
+    Kc, Vc = _rand((B, H, N, d), 86, torch.bfloat16), _rand((B, H, N, d), 87, torch.bfloat16)
+    Kp, Vp = Kc.clone(), Vc.clone()
+    for b in range(B):
+        Kp[b][:, idx[b].long()] = float("nan")
+        Vp[b][:, idx[b].long()] = float("nan")
+        Kp[b][:, idx[b][:5].long()] = 3.0e4
+    O = mar.mar_attn_cache_aware(Q_A, K_A, V_A, Kp, Vp, idx)
+    O_ref, _ = oracle.cache_aware(Q_A, K_A, V_A, Kc, Vc, idx)
+    P.assert_close(O, O_ref, "bf16", "O_A with poisoned stale rows")
+
+
 def test_cache_aware_reports_bad_indices():
     B, H, N, A, d = 2, 2, 64, 4, 32
     Q_A = _rand((B, H, A, d), 71, torch.float32)
