@@ -10,28 +10,32 @@
 // in blocks of 64 rows straight from the two sources into shared memory with TMA tile
 // loads: first the fresh active rows (cache-aware) or all rows (full attention), then,
 // for cache-aware attention, the cache slab of the (b, h) in position order. Cache rows
-// of active positions hold stale values: they are masked out of the softmax by a bitmap
-// of the active positions built in the CTA, so they never contribute (they are read,
-// costing A/N extra bytes, because one tile load per 64 rows runs at the TMA unit's
-// full rate while a per-row gather is bound by its request rate).
+// of active positions hold stale values: a bitmap of the active positions masks them out
+// of the softmax and their V rows are cleared in shared memory, so they never contribute
+// (they are read, costing A/N extra bytes, because one tile load per 64 rows runs at the
+// TMA unit's full rate while a per-row gather is bound by its request rate).
 //
-// CTA = one (b, h) and 128 query rows; 6 warps:
+// Persistent CTAs (two per SM): CTA c processes the tiles c, c + grid, ... where a tile
+// is one (b, h) and 128 query rows. 7 warps:
 //   warps 0-3  softmax + epilogue; thread t owns query row t (tensor-memory lane t)
-//   warp 4     TMA producer (Q once; K/V blocks through a ring of stages)
-//   warp 5     MMA issuer (one lane):  S_j = Q K_j^T  (M=128, N=64, K=d, K-major operands)
-//                                       O  += P_j V_j  (M=128, N=d, K=64, P from TMEM,
+//   warp 4     TMA producer: Q of each tile (double-buffered) and the K/V blocks of all
+//              tiles through one ring of stages, running ahead across tile boundaries
+//   warp 5     MMA issuer (one lane):  S_g = Q K_g^T  (M=128, N=64, K=d, K-major operands)
+//                                       O  += P_g V_g  (M=128, N=d, K=64, P from TMEM,
 //                                                       V MN-major)
-//              It polls its barriers and issues whichever MMA is ready: PV_j as soon as
-//              P_j is written, S_{j+2} as soon as PV_j has released its buffer.
-// Tensor memory (256 columns): two S buffers of 64 columns (S_j, S_{j+1}), each
-// overwritten in place by P_j as packed bf16 pairs, and O (d columns) accumulated by the
-// MMAs across all blocks. While the softmax warps turn S_j into P_j, the tensor core
-// already computes S_{j+1}.
+//              It polls its barriers and issues whichever MMA is ready: PV_g as soon as
+//              P_g is written, S_{g+2} as soon as PV_g has released its buffer.
+//   warp 6     index warp: bitmap of the active positions of each tile (double-
+//              buffered) and the fused cache scatter.
+// g numbers the key blocks of a CTA across its tiles; every ring (stages, S/P buffers,
+// Q buffers, bitmaps) is indexed by g or by the tile count, and every barrier is waited
+// one phase at a time, in order, so parity waits are exact.
 //
-// Online softmax with a lazy rescale: each row keeps the max m it used for its P values;
-// a block whose row max exceeds m by more than 8 (base-2 units) raises m and rescales
-// O and l by 2^(m_old - m_new) in tensor memory; otherwise P = 2^(s - m) <= 2^8 and no
-// rescale is needed. O / l at the end is the same softmax-weighted sum either way.
+// Tensor memory (256 columns): two S buffers of 64 columns, each overwritten in place by
+// P as packed bf16 pairs, and O (d columns) accumulated across the blocks of a tile.
+// Online softmax with a lazy rescale: a row keeps the max m used for its P values; a
+// block whose row max exceeds m by more than 8 (base-2 units) raises m and rescales O
+// and l by 2^(m_old - m_new); otherwise P = 2^(s - m) <= 2^8 and nothing is rescaled.
 // d = 80 keeps columns 64..79 of every tile in a separate 32-byte-swizzled region:
 // QK^T takes 4 k-steps on the 128-byte-swizzled part and 1 on the tail; PV issues an
 // N=64 and an N=16 MMA per k-step. Every wait is bounded (tc5.cuh).
@@ -47,29 +51,40 @@ namespace {
 
 using namespace tc5;
 
-constexpr int BM = 128;          // query rows per CTA
-constexpr int BN = 64;           // key slots per block
-constexpr int kThreads = 192;
+constexpr int BM = 128;          // query rows per tile
+constexpr int BN = 64;           // keys per block
+constexpr int kThreads = 224;    // 7 warps
 constexpr uint32_t kTmemCols = 256;
 constexpr float kRescale = 8.f;  // lazy-rescale threshold (base-2 units)
 
 template <int D>
 struct Cfg {
-    static constexpr int DB = D - 64;                         // tail columns (0 or 16)
+    static constexpr int DB = D - 64;                                   // tail columns (0 or 16)
     static constexpr int kStages = (D == 64) ? 4 : 3;
-    static constexpr uint32_t kQa = BM * 128, kQb = BM * DB * 2;            // Q tile parts
-    static constexpr uint32_t kKa = BN * 128, kKb = BN * DB * 2;            // one K (or V) block
-    static constexpr uint32_t kKV = 2 * (kKa + kKb);                        // K + V of one block
-    // shared-memory offsets (1024-aligned pieces)
-    static constexpr uint32_t oQa = 0, oQb = oQa + kQa;
-    static constexpr uint32_t oStage = ((oQb + kQb + 1023) / 1024) * 1024;
+    static constexpr uint32_t kQa = BM * 128, kQb = BM * DB * 2;        // Q tile parts
+    static constexpr uint32_t kQBytes = ((kQa + kQb + 1023) / 1024) * 1024;
+    static constexpr uint32_t kKa = BN * 128, kKb = BN * DB * 2;        // one K (or V) block
+    static constexpr uint32_t kKV = 2 * (kKa + kKb);                    // K + V of one block
     static constexpr uint32_t kStageBytes = ((kKV + 1023) / 1024) * 1024;
+    // shared memory: Q[2] | stages | barriers | bitmaps
+    static constexpr uint32_t oQ = 0;
+    static constexpr uint32_t oStage = 2 * kQBytes;
     static constexpr uint32_t oBars = oStage + kStages * kStageBytes;
-    // stage layout: Ka | Va | Kb | Vb
+    // Q buffer layout: Qa | Qb; stage layout: Ka | Va | Kb | Vb
     static constexpr uint32_t sKa = 0, sVa = kKa, sKb = 2 * kKa, sVb = 2 * kKa + kKb;
 };
 
-enum Bar { Q_FULL = 0, S_FULL = 1, P_FULL = 3, O_DONE = 5, KV_FULL = 7 };  // then KV_EMPTY
+// barrier slots
+enum Bar {
+    Q_FULL = 0,      // [2]
+    Q_EMPTY = 2,     // [2]
+    S_FULL = 4,      // [2]
+    P_FULL = 6,      // [2]
+    O_DONE = 8,      // [2] PV of block g -> O_DONE[g & 1]
+    BM_FULL = 10,    // [2]
+    BM_EMPTY = 12,   // [2]
+    KV_FULL = 14     // [S], then KV_EMPTY [S]
+};
 
 template <int D>
 struct Tc5Params {
@@ -80,6 +95,7 @@ struct Tc5Params {
     CUtensorMap mVca, mVcb;
     AttnParams a;
     int gather;
+    int n_tiles;
 };
 
 MAR_DEVINL uint32_t lane_addr(uint32_t tm, int warp, int col) {
@@ -87,7 +103,7 @@ MAR_DEVINL uint32_t lane_addr(uint32_t tm, int warp, int col) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2) attn_tc5_kernel(const __grid_constant__ Tc5Params<D> P) {
+__global__ void __maxnreg__(144) attn_tc5_kernel(const __grid_constant__ Tc5Params<D> P) {
     using C = Cfg<D>;
     constexpr int S = C::kStages;
     const AttnParams &p = P.a;
@@ -98,23 +114,31 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc5_kernel(const __grid_cons
     uint64_t *kv_empty = bars + KV_FULL + S;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + KV_FULL + 2 * S);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    uint32_t *bitmap = reinterpret_cast<uint32_t *>(tmem_slot + 4);  // active positions
+    const int bm_words = 2 * ((p.N + BN - 1) / BN);  // one bitmap: whole 64-position blocks
+    uint32_t *bitmaps = reinterpret_cast<uint32_t *>(tmem_slot + 4);  // [2][bm_words]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nqt = (p.nq + BM - 1) / BM;
-    const int qt = blockIdx.x % nqt, bh = blockIdx.x / nqt, b = bh / p.H;
-    const int q0 = qt * BM;
+    const int my_tiles = (P.n_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+
+    // key blocks per tile: nd blocks of dense rows (the fresh active rows, or all rows of
+    // K/V), then for cache-aware attention nc blocks of the cache slab in position order
+    const int nd = (p.n_dense + BN - 1) / BN;
+    const int nc = (P.gather && p.A < p.N) ? (p.N + BN - 1) / BN : 0;
+    const int nblk = nd + nc;
 
     if (warp == 4) tmem_alloc(tmem_slot, kTmemCols);
     if (tid == 0) {
         *abort_flag = 0;
-        mbar_init(&bars[Q_FULL], 1);
         for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[Q_FULL + i], 1);
+            mbar_init(&bars[Q_EMPTY + i], 1);
             mbar_init(&bars[S_FULL + i], 1);
             mbar_init(&bars[P_FULL + i], 4);
+            mbar_init(&bars[O_DONE + i], 1);
+            mbar_init(&bars[BM_FULL + i], 1);
+            mbar_init(&bars[BM_EMPTY + i], 4);
         }
-        mbar_init(&bars[O_DONE], 1);
-        mbar_init(&bars[O_DONE + 1], 1);
         for (int i = 0; i < S; ++i) {
             mbar_init(&bars[KV_FULL + i], 1);
             mbar_init(&kv_empty[i], 1);
@@ -124,55 +148,39 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc5_kernel(const __grid_cons
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 4 && lane == 0) {  // Q does not depend on the cached list: start it now
-        tma_prefetch_desc(&P.mQa);
-        mbar_arrive_expect_tx(&bars[Q_FULL], C::kQa + C::kQb);
-        tma_load_3d(sm + C::oQa, &P.mQa, 0, q0, bh, &bars[Q_FULL]);
-        if constexpr (C::DB > 0) tma_load_3d(sm + C::oQb, &P.mQb, 64, q0, bh, &bars[Q_FULL]);
-    }
-    if (P.gather) {
-        // bitmap of the active positions of row b (their cache rows are stale)
-        const int words = 2 * ((p.N + BN - 1) / BN);
-        for (int w = tid; w < words; w += kThreads) bitmap[w] = 0u;
-        __syncthreads();
-        uint32_t bad = 0;
-        for (int a = tid; a < p.A; a += kThreads) {
-            const int pos = p.idx[(int64_t)b * p.A + a];
-            if (pos < 0 || pos >= p.N) {
-                bad |= MAR_STATUS_INDEX_RANGE;
-                continue;
-            }
-            const uint32_t old = atomicOr(&bitmap[pos >> 5], 1u << (pos & 31));
-            if (old & (1u << (pos & 31))) bad |= MAR_STATUS_INDEX_DUP;
-        }
-        if (bad) report(p.status, bad);
-    }
-    __syncthreads();
     const uint32_t tm = *tmem_slot;
     const uint32_t tmS0 = tm, tmO = tm + 128;
-
-    // key blocks: nd blocks of dense rows (the fresh active rows, or all rows of K/V), then
-    // for cache-aware attention nc blocks of the cache slab in position order
-    const int nd = (p.n_dense + BN - 1) / BN;
-    const int nc = (P.gather && p.A < p.N) ? (p.N + BN - 1) / BN : 0;
-    const int nblk = nd + nc;
 
     if (warp == 4) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            for (int j = 0; j < nblk; ++j) {
-                const int st = j % S;
-                if (!mbar_wait(&kv_empty[st], ((j / S) & 1) ^ 1, p.status, abort_flag)) break;
-                unsigned char *stg = sm + C::oStage + st * C::kStageBytes;
-                uint64_t *fb = &bars[KV_FULL + st];
-                mbar_arrive_expect_tx(fb, C::kKV);
-                const bool dense = j < nd;
-                const int row = (dense ? j : j - nd) * BN;
-                tma_load_3d(stg + C::sKa, dense ? &P.mKa : &P.mKca, 0, row, bh, fb);
-                tma_load_3d(stg + C::sVa, dense ? &P.mVa : &P.mVca, 0, row, bh, fb);
-                if constexpr (C::DB > 0) {
-                    tma_load_3d(stg + C::sKb, dense ? &P.mKb : &P.mKcb, 64, row, bh, fb);
-                    tma_load_3d(stg + C::sVb, dense ? &P.mVb : &P.mVcb, 64, row, bh, fb);
+            tma_prefetch_desc(&P.mQa);
+            tma_prefetch_desc(&P.mKa);
+            tma_prefetch_desc(&P.mVa);
+            bool ok = true;
+            for (int it = 0; ok && it < my_tiles; ++it) {
+                const int tile = (int)blockIdx.x + it * (int)gridDim.x;
+                const int bh = tile / nqt, q0 = (tile % nqt) * BM;
+                const int qb = it & 1;
+                if (!(ok = mbar_wait(&bars[Q_EMPTY + qb], ((it >> 1) & 1) ^ 1, p.status, abort_flag))) break;
+                unsigned char *sq = sm + C::oQ + qb * C::kQBytes;
+                mbar_arrive_expect_tx(&bars[Q_FULL + qb], C::kQa + C::kQb);
+                tma_load_3d(sq, &P.mQa, 0, q0, bh, &bars[Q_FULL + qb]);
+                if constexpr (C::DB > 0) tma_load_3d(sq + C::kQa, &P.mQb, 64, q0, bh, &bars[Q_FULL + qb]);
+                for (int j = 0; j < nblk; ++j) {
+                    const int g = it * nblk + j, st = g % S;
+                    if (!(ok = mbar_wait(&kv_empty[st], ((g / S) & 1) ^ 1, p.status, abort_flag))) break;
+                    unsigned char *stg = sm + C::oStage + st * C::kStageBytes;
+                    uint64_t *fb = &bars[KV_FULL + st];
+                    mbar_arrive_expect_tx(fb, C::kKV);
+                    const bool dense = j < nd;
+                    const int row = (dense ? j : j - nd) * BN;
+                    tma_load_3d(stg + C::sKa, dense ? &P.mKa : &P.mKca, 0, row, bh, fb);
+                    tma_load_3d(stg + C::sVa, dense ? &P.mVa : &P.mVca, 0, row, bh, fb);
+                    if constexpr (C::DB > 0) {
+                        tma_load_3d(stg + C::sKb, dense ? &P.mKb : &P.mKcb, 64, row, bh, fb);
+                        tma_load_3d(stg + C::sVb, dense ? &P.mVb : &P.mVcb, 64, row, bh, fb);
+                    }
                 }
             }
         }
@@ -183,42 +191,47 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc5_kernel(const __grid_cons
             const uint32_t idS = idesc_bf16(BM, BN, 0, 0);
             const uint32_t idOa = idesc_bf16(BM, 64, 0, 1);
             const uint32_t idOb = idesc_bf16(BM, 16, 0, 1);
-            const uint64_t dQa = smem_desc(sm + C::oQa, 16, 1024, Swz::B128);
-            const uint64_t dQb = smem_desc(sm + C::oQb, 16, 256, Swz::B32);
-            bool ok = mbar_wait(&bars[Q_FULL], 0, p.status, abort_flag);
+            const int total = my_tiles * nblk;
             int next_s = 0, next_pv = 0;
             uint32_t idle = 0;
-            while (ok && next_pv < nblk) {
+            bool ok = true;
+            while (ok && next_pv < total) {
                 bool progress = false;
-                // S_j: its K block has landed and PV_{j-2} has released S/P buffer j & 1.
-                // Each barrier is tested one phase at a time, in order, so parities are exact.
-                if (next_s < nblk && next_s < next_pv + 2) {
-                    const int j = next_s;
-                    bool ready = mbar_try_wait(&bars[KV_FULL + j % S], (j / S) & 1);
-                    if (ready && j >= 2) ready = mbar_try_wait(&bars[O_DONE + (j & 1)], ((j - 2) >> 1) & 1);
+                // S_g: Q of its tile has landed, its K block has landed, and PV_{g-2} has
+                // released S/P buffer g & 1
+                if (next_s < total && next_s < next_pv + 2) {
+                    const int g = next_s, it = g / nblk, j = g - it * nblk;
+                    bool ready = mbar_try_wait(&bars[KV_FULL + g % S], (g / S) & 1);
+                    if (ready && g >= 2) ready = mbar_try_wait(&bars[O_DONE + (g & 1)], ((g - 2) >> 1) & 1);
+                    if (ready && j == 0) ready = mbar_try_wait(&bars[Q_FULL + (it & 1)], (it >> 1) & 1);
                     if (ready) {
                         tc_fence_after();
-                        const unsigned char *stg = sm + C::oStage + (j % S) * C::kStageBytes;
+                        const unsigned char *sq = sm + C::oQ + (it & 1) * C::kQBytes;
+                        const unsigned char *stg = sm + C::oStage + (g % S) * C::kStageBytes;
+                        const uint64_t dQa = smem_desc(sq, 16, 1024, Swz::B128);
                         const uint64_t dKa = smem_desc(stg + C::sKa, 16, 1024, Swz::B128);
-                        const uint32_t dst = tmS0 + 64 * (j & 1);
+                        const uint32_t dst = tmS0 + 64 * (g & 1);
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
                             mma_ss(dst, desc_advance(dQa, 32 * k), desc_advance(dKa, 32 * k), idS, k > 0);
-                        if constexpr (C::DB > 0) mma_ss(dst, dQb, smem_desc(stg + C::sKb, 16, 256, Swz::B32), idS, 1);
-                        mma_commit(&bars[S_FULL + (j & 1)]);
+                        if constexpr (C::DB > 0)
+                            mma_ss(dst, smem_desc(sq + C::kQa, 16, 256, Swz::B32),
+                                   smem_desc(stg + C::sKb, 16, 256, Swz::B32), idS, 1);
+                        mma_commit(&bars[S_FULL + (g & 1)]);
+                        if (j == nblk - 1) mma_commit(&bars[Q_EMPTY + (it & 1)]);  // Q buffer reusable
                         ++next_s;
                         progress = true;
                     }
                 }
-                // PV_j: P_j has been written over S_j
+                // PV_g: P_g has been written over S_g
                 if (next_pv < next_s) {
-                    const int j = next_pv;
-                    if (mbar_try_wait(&bars[P_FULL + (j & 1)], (j >> 1) & 1)) {
+                    const int g = next_pv, j = g % nblk;
+                    if (mbar_try_wait(&bars[P_FULL + (g & 1)], (g >> 1) & 1)) {
                         tc_fence_after();
-                        const unsigned char *stg = sm + C::oStage + (j % S) * C::kStageBytes;
+                        const unsigned char *stg = sm + C::oStage + (g % S) * C::kStageBytes;
                         const uint64_t dVa = smem_desc(stg + C::sVa, 1024, 1024, Swz::B128);
                         const uint64_t dVb = smem_desc(stg + C::sVb, 256, 256, Swz::B32);
-                        const uint32_t pcol = tmS0 + 64 * (j & 1);
+                        const uint32_t pcol = tmS0 + 64 * (g & 1);
 #pragma unroll
                         for (int k = 0; k < BN / 16; ++k) {
                             const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
@@ -226,8 +239,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc5_kernel(const __grid_cons
                             if constexpr (C::DB > 0)
                                 mma_ts(tmO + 64, pcol + 8 * k, desc_advance(dVb, 512 * k), idOb, acc);
                         }
-                        mma_commit(&bars[O_DONE + (j & 1)]);
-                        mma_commit(&kv_empty[j % S]);
+                        mma_commit(&bars[O_DONE + (g & 1)]);
+                        mma_commit(&kv_empty[g % S]);
                         ++next_pv;
                         progress = true;
                     }
@@ -244,156 +257,198 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc5_kernel(const __grid_cons
             }
         }
         __syncwarp();
+    } else if (warp == 6) {
+        // ------------------------------------------------------------ index warp
+        if (P.gather) {
+            for (int it = 0; it < my_tiles; ++it) {
+                const int tile = (int)blockIdx.x + it * (int)gridDim.x;
+                const int bh = tile / nqt, qt = tile % nqt, b = bh / p.H;
+                const int bb = it & 1;
+                uint32_t *bm = bitmaps + bb * bm_words;
+                if (nc > 0) {  // with no cache blocks (A == N) nothing reads the bitmap
+                    if (!mbar_wait(&bars[BM_EMPTY + bb], ((it >> 1) & 1) ^ 1, p.status, abort_flag)) break;
+                    for (int w = lane; w < bm_words; w += 32) bm[w] = 0u;
+                    __syncwarp();
+                    uint32_t bad = 0;
+                    for (int a = lane; a < p.A; a += 32) {
+                        const int pos = p.idx[(int64_t)b * p.A + a];
+                        if (pos < 0 || pos >= p.N) {
+                            bad |= MAR_STATUS_INDEX_RANGE;
+                            continue;
+                        }
+                        const uint32_t old = atomicOr(&bm[pos >> 5], 1u << (pos & 31));
+                        if (old & (1u << (pos & 31))) bad |= MAR_STATUS_INDEX_DUP;
+                    }
+                    if (bad) report(p.status, bad);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[BM_FULL + bb]);
+                }
+                if (p.fuse_scatter && qt == 0) {
+                    // Fresh K_A/V_A rows -> cache rows of the active positions. No query of
+                    // this launch uses those rows (they are masked as stale).
+                    const bf16 *Kd = static_cast<const bf16 *>(p.Kd);
+                    const bf16 *Vd = static_cast<const bf16 *>(p.Vd);
+                    bf16 *Kc = static_cast<bf16 *>(p.Kc);
+                    bf16 *Vc = static_cast<bf16 *>(p.Vc);
+                    for (int t = lane; t < p.A * (D / 8); t += 32) {
+                        const int a = t / (D / 8), c = t % (D / 8);
+                        const int pos = p.idx[(int64_t)b * p.A + a];
+                        if (pos < 0 || pos >= p.N) continue;
+                        const int64_t src = ((int64_t)bh * p.A + a) * D + 8 * c;
+                        const int64_t dst = ((int64_t)bh * p.N + pos) * D + 8 * c;
+                        *reinterpret_cast<uint4 *>(Kc + dst) = *reinterpret_cast<const uint4 *>(Kd + src);
+                        *reinterpret_cast<uint4 *>(Vc + dst) = *reinterpret_cast<const uint4 *>(Vd + src);
+                    }
+                }
+            }
+        }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
-        if (P.gather && p.fuse_scatter && qt == 0) {
-            // Fresh K_A/V_A rows -> cache rows of the active positions. No query of this
-            // launch uses those rows (they are masked as stale), so the order is free.
-            const bf16 *Kd = static_cast<const bf16 *>(p.Kd);
-            const bf16 *Vd = static_cast<const bf16 *>(p.Vd);
-            bf16 *Kc = static_cast<bf16 *>(p.Kc);
-            bf16 *Vc = static_cast<bf16 *>(p.Vc);
-            for (int t = tid; t < p.A * (D / 8); t += 128) {
-                const int a = t / (D / 8), c = t % (D / 8);
-                const int pos = p.idx[(int64_t)b * p.A + a];
-                if (pos < 0 || pos >= p.N) continue;
-                const int64_t src = ((int64_t)bh * p.A + a) * D + 8 * c;
-                const int64_t dst = ((int64_t)bh * p.N + pos) * D + 8 * c;
-                *reinterpret_cast<uint4 *>(Kc + dst) = *reinterpret_cast<const uint4 *>(Kd + src);
-                *reinterpret_cast<uint4 *>(Vc + dst) = *reinterpret_cast<const uint4 *>(Vd + src);
-            }
-        }
         const float sl2 = p.scale * kLog2e;
-        const bool live = (q0 + 32 * warp) < p.nq;  // warp-uniform: some row of this warp is real
-        float m_use = 0.f, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < nblk; ++j) {
-            const int buf = j & 1;
-            if (!mbar_wait(&bars[S_FULL + buf], (j >> 1) & 1, p.status, abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            // slots of this block that are keys: dense rows below n_dense; cache rows below
-            // N whose position is not active (active positions hold stale cache rows)
-            uint64_t valid, stale = 0ull;
-            if (j < nd) {
-                const int r = p.n_dense - j * BN;
-                valid = r >= 64 ? ~0ull : ((1ull << r) - 1ull);
-            } else {
-                const int pos0 = (j - nd) * BN;
-                stale = (uint64_t)bitmap[pos0 >> 5] | ((uint64_t)bitmap[(pos0 >> 5) + 1] << 32);
-                valid = ~stale;
-                const int r = p.N - pos0;
-                if (r < 64) {
-                    valid &= (1ull << r) - 1ull;
-                    stale &= (1ull << r) - 1ull;
-                }
-            }
-            if (stale) {
-                // Their P is 0, but 0 x NaN is NaN: clear the stale V rows in shared memory so
-                // that whatever a stale row holds cannot reach O. Whole rows are cleared, so
-                // the swizzle inside a row does not matter.
-                unsigned char *stg = sm + C::oStage + (j % S) * C::kStageBytes;
-                for (int t = tid; t < BN * 8; t += 128)
-                    if ((stale >> (t >> 3)) & 1ull) *reinterpret_cast<uint4 *>(stg + C::sVa + 16 * t) = make_uint4(0, 0, 0, 0);
-                if constexpr (C::DB > 0) {
-                    for (int t = tid; t < BN * 2; t += 128)
-                        if ((stale >> (t >> 1)) & 1ull) *reinterpret_cast<uint4 *>(stg + C::sVb + 16 * t) = make_uint4(0, 0, 0, 0);
-                }
-                fence_proxy_async_smem();
-            }
-            if (live) {
-                float v[64];
-                tmem_ld64(lane_addr(tmS0, warp, 64 * buf), v);
-                float mx = -INFINITY;
-                if (valid == ~0ull) {
-#pragma unroll
-                    for (int i = 0; i < 64; ++i) {
-                        v[i] *= sl2;
-                        mx = fmaxf(mx, v[i]);
-                    }
+        for (int it = 0; ok && it < my_tiles; ++it) {
+            const int tile = (int)blockIdx.x + it * (int)gridDim.x;
+            const int bh = tile / nqt, q0 = (tile % nqt) * BM;
+            const bool live = (q0 + 32 * warp) < p.nq;  // warp-uniform: some row of this warp is real
+            const uint32_t *bm = bitmaps + (it & 1) * bm_words;
+            float m_use = 0.f, l = 0.f;
+            for (int j = 0; j < nblk; ++j) {
+                const int g = it * nblk + j, buf = g & 1;
+                if (j == nd && nc > 0 &&
+                    !(ok = mbar_wait(&bars[BM_FULL + (it & 1)], (it >> 1) & 1, p.status, abort_flag)))
+                    break;
+                if (!(ok = mbar_wait(&bars[S_FULL + buf], (g >> 1) & 1, p.status, abort_flag))) break;
+                tc_fence_after();
+                // slots of this block that are keys: dense rows below n_dense; cache rows below
+                // N whose position is not active (active positions hold stale cache rows)
+                uint64_t valid, stale = 0ull;
+                if (j < nd) {
+                    const int r = p.n_dense - j * BN;
+                    valid = r >= 64 ? ~0ull : ((1ull << r) - 1ull);
                 } else {
-#pragma unroll
-                    for (int i = 0; i < 64; ++i) {
-                        v[i] = ((valid >> i) & 1ull) ? v[i] * sl2 : -INFINITY;
-                        mx = fmaxf(mx, v[i]);
+                    const int pos0 = (j - nd) * BN;
+                    stale = (uint64_t)bm[pos0 >> 5] | ((uint64_t)bm[(pos0 >> 5) + 1] << 32);
+                    valid = ~stale;
+                    const int r = p.N - pos0;
+                    if (r < 64) {
+                        valid &= (1ull << r) - 1ull;
+                        stale &= (1ull << r) - 1ull;
                     }
                 }
-                bool rescale = false;
-                float factor = 1.f;
-                if (j == 0) {
-                    m_use = (mx == -INFINITY) ? 0.f : mx;
-                } else if (mx > m_use + kRescale) {
-                    factor = fast_exp2(m_use - mx);
-                    m_use = mx;
-                    rescale = true;
+                if (stale) {
+                    // Their P is 0, but 0 x NaN is NaN: clear the stale V rows in shared memory
+                    // so that whatever a stale row holds cannot reach O. Whole rows are cleared,
+                    // so the swizzle inside a row does not matter.
+                    unsigned char *stg = sm + C::oStage + (g % S) * C::kStageBytes;
+                    for (int t = tid; t < BN * 8; t += 128)
+                        if ((stale >> (t >> 3)) & 1ull)
+                            *reinterpret_cast<uint4 *>(stg + C::sVa + 16 * t) = make_uint4(0, 0, 0, 0);
+                    if constexpr (C::DB > 0) {
+                        for (int t = tid; t < BN * 2; t += 128)
+                            if ((stale >> (t >> 1)) & 1ull)
+                                *reinterpret_cast<uint4 *>(stg + C::sVb + 16 * t) = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
                 }
-                if (__any_sync(0xffffffffu, rescale)) {
-                    // O holds sum_{i<j} P_i V_i; wait for PV_{j-1} and scale the rows that
-                    // raised their max (the other rows use factor 1)
-                    if (!mbar_wait(&bars[O_DONE + ((j - 1) & 1)], ((j - 1) >> 1) & 1, p.status, abort_flag)) {
-                        ok = false;
-                    } else {
-                        tc_fence_after();
+                if (live) {
+                    float v[64];
+                    tmem_ld64(lane_addr(tmS0, warp, 64 * buf), v);
+                    float mx = -INFINITY;
+                    if (valid == ~0ull) {
 #pragma unroll
-                        for (int c0 = 0; c0 < D; c0 += 16) {
-                            float o[16];
-                            tmem_ld16(lane_addr(tmO, warp, c0), o);
-                            uint32_t w[16];
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(o[i] * factor);
-                            tmem_st16(lane_addr(tmO, warp, c0), w);
+                        for (int i = 0; i < 64; ++i) {
+                            v[i] *= sl2;
+                            mx = fmaxf(mx, v[i]);
                         }
-                        l *= factor;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) {
+                            v[i] = ((valid >> i) & 1ull) ? v[i] * sl2 : -INFINITY;
+                            mx = fmaxf(mx, v[i]);
+                        }
+                    }
+                    bool rescale = false;
+                    float factor = 1.f;
+                    if (j == 0) {
+                        m_use = (mx == -INFINITY) ? 0.f : mx;
+                    } else if (mx > m_use + kRescale) {
+                        factor = fast_exp2(m_use - mx);
+                        m_use = mx;
+                        rescale = true;
+                    }
+                    if (__any_sync(0xffffffffu, rescale)) {
+                        // O holds the tile's sum over earlier blocks; wait for PV_{g-1} and
+                        // scale the rows that raised their max (the others use factor 1)
+                        ok = mbar_wait(&bars[O_DONE + ((g - 1) & 1)], ((g - 1) >> 1) & 1, p.status, abort_flag);
+                        if (ok) {
+                            tc_fence_after();
+#pragma unroll
+                            for (int c0 = 0; c0 < D; c0 += 16) {
+                                float o[16];
+                                tmem_ld16(lane_addr(tmO, warp, c0), o);
+                                uint32_t w[16];
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(o[i] * factor);
+                                tmem_st16(lane_addr(tmO, warp, c0), w);
+                            }
+                            l *= factor;
+                        }
+                    }
+                    float rs = 0.f;
+                    uint32_t w0[16], w1[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = fast_exp2(v[2 * i] - m_use), p1 = fast_exp2(v[2 * i + 1] - m_use);
+                        const float p2 = fast_exp2(v[32 + 2 * i] - m_use), p3 = fast_exp2(v[33 + 2 * i] - m_use);
+                        rs += (p0 + p1) + (p2 + p3);
+                        w0[i] = pack_bf16x2(p0, p1);
+                        w1[i] = pack_bf16x2(p2, p3);
+                    }
+                    l += rs;
+                    tmem_st16(lane_addr(tmS0, warp, 64 * buf), w0);
+                    tmem_st16(lane_addr(tmS0, warp, 64 * buf + 16), w1);
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bars[P_FULL + buf]);
+                    if (j == nblk - 1 && nc > 0) mbar_arrive(&bars[BM_EMPTY + (it & 1)]);
+                }
+                if (!ok) break;
+            }
+            if (!ok) break;
+            // PV of the tile's last block was issued after PV_{g-2} finished, so its barrier
+            // phase is exact; MMAs complete in order, so it covers all of the tile's PVs.
+            const int gl = it * nblk + nblk - 1;
+            if (!(ok = mbar_wait(&bars[O_DONE + (gl & 1)], (gl >> 1) & 1, p.status, abort_flag))) break;
+            tc_fence_after();
+            if (live) {
+                const int row = q0 + tid;
+                const float inv = 1.f / l;
+                bf16 *Og = static_cast<bf16 *>(p.O) + ((int64_t)bh * p.nq + row) * D;
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 16) {
+                    float o[16];
+                    tmem_ld16(lane_addr(tmO, warp, c0), o);
+                    if (row < p.nq) {
+                        uint4 u0, u1;
+                        u0.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+                        u0.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+                        u0.z = pack_bf16x2(o[4] * inv, o[5] * inv);
+                        u0.w = pack_bf16x2(o[6] * inv, o[7] * inv);
+                        u1.x = pack_bf16x2(o[8] * inv, o[9] * inv);
+                        u1.y = pack_bf16x2(o[10] * inv, o[11] * inv);
+                        u1.z = pack_bf16x2(o[12] * inv, o[13] * inv);
+                        u1.w = pack_bf16x2(o[14] * inv, o[15] * inv);
+                        *reinterpret_cast<uint4 *>(Og + c0) = u0;
+                        *reinterpret_cast<uint4 *>(Og + c0 + 8) = u1;
                     }
                 }
-                float rs = 0.f;
-                uint32_t w0[16], w1[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float p0 = fast_exp2(v[2 * i] - m_use), p1 = fast_exp2(v[2 * i + 1] - m_use);
-                    const float p2 = fast_exp2(v[32 + 2 * i] - m_use), p3 = fast_exp2(v[33 + 2 * i] - m_use);
-                    rs += (p0 + p1) + (p2 + p3);
-                    w0[i] = pack_bf16x2(p0, p1);
-                    w1[i] = pack_bf16x2(p2, p3);
-                }
-                l += rs;
-                tmem_st16(lane_addr(tmS0, warp, 64 * buf), w0);
-                tmem_st16(lane_addr(tmS0, warp, 64 * buf + 16), w1);
-                tmem_wait_st();
+                if (p.lse && row < p.nq) p.lse[(int64_t)bh * p.nq + row] = (m_use + log2f(l)) * kLn2;
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[P_FULL + buf]);
-            if (!ok) break;
-        }
-        // PV_{nblk-1} was issued after PV_{nblk-3} finished, so its barrier phase is exact;
-        // MMAs complete in order, so its completion covers every earlier PV.
-        if (ok && mbar_wait(&bars[O_DONE + ((nblk - 1) & 1)], ((nblk - 1) >> 1) & 1, p.status, abort_flag) && live) {
-            tc_fence_after();
-            const int row = q0 + tid;
-            const float inv = 1.f / l;
-            bf16 *Og = static_cast<bf16 *>(p.O) + ((int64_t)bh * p.nq + row) * D;
-#pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 16) {
-                float o[16];
-                tmem_ld16(lane_addr(tmO, warp, c0), o);
-                if (row < p.nq) {
-                    uint4 u0, u1;
-                    u0.x = pack_bf16x2(o[0] * inv, o[1] * inv);
-                    u0.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-                    u0.z = pack_bf16x2(o[4] * inv, o[5] * inv);
-                    u0.w = pack_bf16x2(o[6] * inv, o[7] * inv);
-                    u1.x = pack_bf16x2(o[8] * inv, o[9] * inv);
-                    u1.y = pack_bf16x2(o[10] * inv, o[11] * inv);
-                    u1.z = pack_bf16x2(o[12] * inv, o[13] * inv);
-                    u1.w = pack_bf16x2(o[14] * inv, o[15] * inv);
-                    *reinterpret_cast<uint4 *>(Og + c0) = u0;
-                    *reinterpret_cast<uint4 *>(Og + c0 + 8) = u1;
-                }
-            }
-            if (p.lse && row < p.nq) p.lse[(int64_t)bh * p.nq + row] = (m_use + log2f(l)) * kLn2;
+            // The next tile's first PV overwrites O only after P of its first block, which
+            // this warp group writes after the reads above have completed.
         }
     }
     tc_fence_before();
@@ -410,6 +465,18 @@ bool map3(CUtensorMap *m, const void *ptr, int rows, int bh, uint32_t boxw, uint
                          boxw == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B);
 }
 
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!cache[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 148;
+    }
+    return cache[dev];
+}
+
 template <int D>
 cudaError_t launch(const AttnParams &p, cudaStream_t s) {
     using C = Cfg<D>;
@@ -418,7 +485,7 @@ cudaError_t launch(const AttnParams &p, cudaStream_t s) {
     P.a = p;
     P.gather = p.idx ? 1 : 0;
     const int bh = p.B * p.H;
-    const uint32_t tw = D == 64 ? 64 : 16;  // tail box width (unused for d = 64)
+    const uint32_t tw = D == 64 ? 64 : 16;  // tail box width (the tail maps are unused for d = 64)
     bool ok = map3<D>(&P.mQa, p.Q, p.nq, bh, 64, BM) && map3<D>(&P.mQb, p.Q, p.nq, bh, tw, BM);
     ok = ok && map3<D>(&P.mKa, p.Kd, p.n_dense, bh, 64, BN) && map3<D>(&P.mKb, p.Kd, p.n_dense, bh, tw, BN);
     ok = ok && map3<D>(&P.mVa, p.Vd, p.n_dense, bh, 64, BN) && map3<D>(&P.mVb, p.Vd, p.n_dense, bh, tw, BN);
@@ -429,12 +496,15 @@ cudaError_t launch(const AttnParams &p, cudaStream_t s) {
         P.mKca = P.mKa; P.mKcb = P.mKb; P.mVca = P.mVa; P.mVcb = P.mVb;
     }
     if (!ok) return cudaErrorInvalidValue;
+    const long long tiles = (long long)((p.nq + BM - 1) / BM) * bh;
+    if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+    P.n_tiles = (int)tiles;
     size_t smem = 1024 + C::oBars + 8 * (KV_FULL + 2 * C::kStages) + 16;
-    if (P.gather) smem += sizeof(uint32_t) * 2 * ((p.N + BN - 1) / BN);
+    smem += sizeof(uint32_t) * 2 * 2 * ((p.N + BN - 1) / BN);  // two bitmaps
     cudaError_t e = ensure_smem(attn_tc5_kernel<D>, smem, configured);
     if (e != cudaSuccess) return e;
-    const long long blocks = (long long)((p.nq + BM - 1) / BM) * bh;
-    attn_tc5_kernel<D><<<(unsigned)blocks, kThreads, smem, s>>>(P);
+    const long long grid = tiles < 2LL * sm_count() ? tiles : 2LL * sm_count();
+    attn_tc5_kernel<D><<<(unsigned)grid, kThreads, smem, s>>>(P);
     return cudaGetLastError();
 }
 
