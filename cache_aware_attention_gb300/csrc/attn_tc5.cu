@@ -15,12 +15,13 @@
 // (they are read, costing A/N extra bytes, because one tile load per 64 rows runs at the
 // TMA unit's full rate while a per-row gather is bound by its request rate).
 //
-// Persistent CTAs (two per SM): CTA c processes the tiles c, c + grid, ... where a tile
-// is one (b, h) and 128 query rows. 7 warps:
+// Persistent CTAs (two per SM; 7 warps x at most 128 registers, so that 14 warps fit the
+// four 16K-register sub-partitions of an SM): CTA c processes the tiles c, c + grid, ...
+// where a tile is one (b, h) and 128 query rows. 7 warps:
 //   warps 0-3  softmax + epilogue; thread t owns query row t (tensor-memory lane t)
 //   warp 4     TMA producer: Q of each tile (double-buffered) and the K/V blocks of all
 //              tiles through one ring of stages, running ahead across tile boundaries
-//   warp 5     MMA issuer (one lane):  S_g = Q K_g^T  (M=128, N=64, K=d, K-major operands)
+//   warp 5     MMA issuer (one elected lane):  S_g = Q K_g^T  (M=128, N=64, K=d, K-major operands)
 //                                       O  += P_g V_g  (M=128, N=d, K=64, P from TMEM,
 //                                                       V MN-major)
 //              It polls its barriers and issues whichever MMA is ready: PV_g as soon as
@@ -103,7 +104,7 @@ MAR_DEVINL uint32_t lane_addr(uint32_t tm, int warp, int col) {
 }
 
 template <int D>
-__global__ void __maxnreg__(144) attn_tc5_kernel(const __grid_constant__ Tc5Params<D> P) {
+__global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Params<D> P) {
     using C = Cfg<D>;
     constexpr int S = C::kStages;
     const AttnParams &p = P.a;
@@ -187,30 +188,35 @@ __global__ void __maxnreg__(144) attn_tc5_kernel(const __grid_constant__ Tc5Para
         __syncwarp();
     } else if (warp == 5) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idS = idesc_bf16(BM, BN, 0, 0);
-            const uint32_t idOa = idesc_bf16(BM, 64, 0, 1);
-            const uint32_t idOb = idesc_bf16(BM, 16, 0, 1);
-            const int total = my_tiles * nblk;
-            int next_s = 0, next_pv = 0;
-            uint32_t idle = 0;
-            bool ok = true;
-            while (ok && next_pv < total) {
-                bool progress = false;
-                // S_g: Q of its tile has landed, its K block has landed, and PV_{g-2} has
-                // released S/P buffer g & 1
-                if (next_s < total && next_s < next_pv + 2) {
-                    const int g = next_s, it = g / nblk, j = g - it * nblk;
-                    bool ready = mbar_try_wait(&bars[KV_FULL + g % S], (g / S) & 1);
-                    if (ready && g >= 2) ready = mbar_try_wait(&bars[O_DONE + (g & 1)], ((g - 2) >> 1) & 1);
-                    if (ready && j == 0) ready = mbar_try_wait(&bars[Q_FULL + (it & 1)], (it >> 1) & 1);
-                    if (ready) {
-                        tc_fence_after();
-                        const unsigned char *sq = sm + C::oQ + (it & 1) * C::kQBytes;
-                        const unsigned char *stg = sm + C::oStage + (g % S) * C::kStageBytes;
-                        const uint64_t dQa = smem_desc(sq, 16, 1024, Swz::B128);
-                        const uint64_t dKa = smem_desc(stg + C::sKa, 16, 1024, Swz::B128);
-                        const uint32_t dst = tmS0 + 64 * (g & 1);
+        // The whole warp runs this loop so that every descriptor is warp-uniform; one
+        // elected lane issues each tcgen05 instruction. (Issuing from a one-lane branch
+        // costs several times more per instruction.) Lane 0's barrier tests are broadcast
+        // so that control flow stays uniform.
+        const uint32_t idS = idesc_bf16(BM, BN, 0, 0);
+        const uint32_t idOa = idesc_bf16(BM, 64, 0, 1);
+        const uint32_t idOb = idesc_bf16(BM, 16, 0, 1);
+        const int total = my_tiles * nblk;
+        int next_s = 0, next_pv = 0;
+        uint32_t idle = 0;
+        bool ok = true;
+        while (ok && next_pv < total) {
+            bool progress = false;
+            // S_g: Q of its tile has landed, its K block has landed, and PV_{g-2} has
+            // released S/P buffer g & 1
+            if (next_s < total && next_s < next_pv + 2) {
+                const int g = next_s, it = g / nblk, j = g - it * nblk;
+                bool ready = mbar_test(&bars[KV_FULL + g % S], (g / S) & 1);
+                if (ready && g >= 2) ready = mbar_test(&bars[O_DONE + (g & 1)], ((g - 2) >> 1) & 1);
+                if (ready && j == 0) ready = mbar_test(&bars[Q_FULL + (it & 1)], (it >> 1) & 1);
+                ready = __shfl_sync(0xffffffffu, ready, 0);
+                if (ready) {
+                    tc_fence_after();
+                    const unsigned char *sq = sm + C::oQ + (it & 1) * C::kQBytes;
+                    const unsigned char *stg = sm + C::oStage + (g % S) * C::kStageBytes;
+                    const uint64_t dQa = smem_desc(sq, 16, 1024, Swz::B128);
+                    const uint64_t dKa = smem_desc(stg + C::sKa, 16, 1024, Swz::B128);
+                    const uint32_t dst = tmS0 + 64 * (g & 1);
+                    if (elect_one()) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
                             mma_ss(dst, desc_advance(dQa, 32 * k), desc_advance(dKa, 32 * k), idS, k > 0);
@@ -219,19 +225,23 @@ __global__ void __maxnreg__(144) attn_tc5_kernel(const __grid_constant__ Tc5Para
                                    smem_desc(stg + C::sKb, 16, 256, Swz::B32), idS, 1);
                         mma_commit(&bars[S_FULL + (g & 1)]);
                         if (j == nblk - 1) mma_commit(&bars[Q_EMPTY + (it & 1)]);  // Q buffer reusable
-                        ++next_s;
-                        progress = true;
                     }
+                    __syncwarp();
+                    ++next_s;
+                    progress = true;
                 }
-                // PV_g: P_g has been written over S_g
-                if (next_pv < next_s) {
-                    const int g = next_pv, j = g % nblk;
-                    if (mbar_try_wait(&bars[P_FULL + (g & 1)], (g >> 1) & 1)) {
-                        tc_fence_after();
-                        const unsigned char *stg = sm + C::oStage + (g % S) * C::kStageBytes;
-                        const uint64_t dVa = smem_desc(stg + C::sVa, 1024, 1024, Swz::B128);
-                        const uint64_t dVb = smem_desc(stg + C::sVb, 256, 256, Swz::B32);
-                        const uint32_t pcol = tmS0 + 64 * (g & 1);
+            }
+            // PV_g: P_g has been written over S_g
+            if (next_pv < next_s) {
+                const int g = next_pv, j = g % nblk;
+                const bool ready = __shfl_sync(0xffffffffu, mbar_test(&bars[P_FULL + (g & 1)], (g >> 1) & 1), 0);
+                if (ready) {
+                    tc_fence_after();
+                    const unsigned char *stg = sm + C::oStage + (g % S) * C::kStageBytes;
+                    const uint64_t dVa = smem_desc(stg + C::sVa, 1024, 1024, Swz::B128);
+                    const uint64_t dVb = smem_desc(stg + C::sVb, 256, 256, Swz::B32);
+                    const uint32_t pcol = tmS0 + 64 * (g & 1);
+                    if (elect_one()) {
 #pragma unroll
                         for (int k = 0; k < BN / 16; ++k) {
                             const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
@@ -241,19 +251,22 @@ __global__ void __maxnreg__(144) attn_tc5_kernel(const __grid_constant__ Tc5Para
                         }
                         mma_commit(&bars[O_DONE + (g & 1)]);
                         mma_commit(&kv_empty[g % S]);
-                        ++next_pv;
-                        progress = true;
                     }
+                    __syncwarp();
+                    ++next_pv;
+                    progress = true;
                 }
-                if (progress) {
-                    idle = 0;
-                } else if (*abort_flag) {
-                    ok = false;
-                } else if (++idle > kSpinLimit) {
+            }
+            if (progress) {
+                idle = 0;
+            } else if (*abort_flag) {
+                ok = false;
+            } else if (++idle > kSpinLimit) {
+                if (lane == 0) {
                     report(p.status, MAR_STATUS_TIMEOUT_BIT);
                     *abort_flag = 1;
-                    ok = false;
                 }
+                ok = false;
             }
         }
         __syncwarp();
@@ -376,9 +389,35 @@ __global__ void __maxnreg__(144) attn_tc5_kernel(const __grid_constant__ Tc5Para
                         m_use = mx;
                         rescale = true;
                     }
+                    // P = 2^(s - m) as bf16 pairs over S, one half at a time
+                    float rs0 = 0.f, rs1 = 0.f;
+                    {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float p0 = fast_exp2(v[2 * i] - m_use), p1 = fast_exp2(v[2 * i + 1] - m_use);
+                            rs0 += p0;
+                            rs1 += p1;
+                            w[i] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16(lane_addr(tmS0, warp, 64 * buf), w);
+                    }
+                    {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float p0 = fast_exp2(v[32 + 2 * i] - m_use), p1 = fast_exp2(v[33 + 2 * i] - m_use);
+                            rs0 += p0;
+                            rs1 += p1;
+                            w[i] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16(lane_addr(tmS0, warp, 64 * buf + 16), w);
+                    }
+                    l = l * factor + (rs0 + rs1);
                     if (__any_sync(0xffffffffu, rescale)) {
                         // O holds the tile's sum over earlier blocks; wait for PV_{g-1} and
-                        // scale the rows that raised their max (the others use factor 1)
+                        // scale the rows that raised their max (the others use factor 1).
+                        // PV_g, which adds this block, is issued only after P_FULL below.
                         ok = mbar_wait(&bars[O_DONE + ((g - 1) & 1)], ((g - 1) >> 1) & 1, p.status, abort_flag);
                         if (ok) {
                             tc_fence_after();
@@ -386,27 +425,12 @@ __global__ void __maxnreg__(144) attn_tc5_kernel(const __grid_constant__ Tc5Para
                             for (int c0 = 0; c0 < D; c0 += 16) {
                                 float o[16];
                                 tmem_ld16(lane_addr(tmO, warp, c0), o);
-                                uint32_t w[16];
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(o[i] * factor);
-                                tmem_st16(lane_addr(tmO, warp, c0), w);
+                                for (int i = 0; i < 16; ++i) o[i] *= factor;
+                                tmem_st16(lane_addr(tmO, warp, c0), o);
                             }
-                            l *= factor;
                         }
                     }
-                    float rs = 0.f;
-                    uint32_t w0[16], w1[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float p0 = fast_exp2(v[2 * i] - m_use), p1 = fast_exp2(v[2 * i + 1] - m_use);
-                        const float p2 = fast_exp2(v[32 + 2 * i] - m_use), p3 = fast_exp2(v[33 + 2 * i] - m_use);
-                        rs += (p0 + p1) + (p2 + p3);
-                        w0[i] = pack_bf16x2(p0, p1);
-                        w1[i] = pack_bf16x2(p2, p3);
-                    }
-                    l += rs;
-                    tmem_st16(lane_addr(tmS0, warp, 64 * buf), w0);
-                    tmem_st16(lane_addr(tmS0, warp, 64 * buf + 16), w1);
                     tmem_wait_st();
                 }
                 tc_fence_before();
@@ -501,7 +525,7 @@ cudaError_t launch(const AttnParams &p, cudaStream_t s) {
     P.n_tiles = (int)tiles;
     size_t smem = 1024 + C::oBars + 8 * (KV_FULL + 2 * C::kStages) + 16;
     smem += sizeof(uint32_t) * 2 * 2 * ((p.N + BN - 1) / BN);  // two bitmaps
-    cudaError_t e = ensure_smem(attn_tc5_kernel<D>, smem, configured);
+    cudaError_t e = ensure_smem(attn_tc5_kernel<D>, smem, configured, /*max_carveout=*/true);
     if (e != cudaSuccess) return e;
     const long long grid = tiles < 2LL * sm_count() ? tiles : 2LL * sm_count();
     attn_tc5_kernel<D><<<(unsigned)grid, kThreads, smem, s>>>(P);

@@ -121,15 +121,20 @@ MAR_DEVINL int build_cached_list(const int32_t *__restrict__ idx, int A, int N,
     return base;
 }
 
-// Raises the dynamic shared memory limit of `func` to `bytes` once per device.
+// Raises the dynamic shared memory limit of `func` to `bytes` once per device. With
+// max_carveout the kernel also asks for the largest shared-memory carveout of the SM, so
+// that as many CTAs as the shared memory allows can be resident (the default carveout
+// can be one step too small for two ~100 KB CTAs).
 template <typename F>
-inline cudaError_t ensure_smem(F *func, size_t bytes, int *configured /* [64] */) {
-    if (bytes <= 48 * 1024) return cudaSuccess;
+inline cudaError_t ensure_smem(F *func, size_t bytes, int *configured /* [64] */, bool max_carveout = false) {
+    if (bytes <= 48 * 1024 && !max_carveout) return cudaSuccess;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 64 && configured[dev] >= (int)bytes) return cudaSuccess;
     e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess && max_carveout)
+        e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess && dev < 64) configured[dev] = (int)bytes;
     return e;
 }
