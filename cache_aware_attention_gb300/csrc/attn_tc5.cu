@@ -15,25 +15,27 @@
 // (they are read, costing A/N extra bytes, because one tile load per 64 rows runs at the
 // TMA unit's full rate while a per-row gather is bound by its request rate).
 //
-// Persistent CTAs (two per SM; 7 warps x at most 128 registers, so that 14 warps fit the
-// four 16K-register sub-partitions of an SM): CTA c processes the tiles c, c + grid, ...
-// where a tile is one (b, h) and 128 query rows. 7 warps:
+// Persistent CTAs (two per SM; 8 warps x at most 128 registers, so that the two CTAs'
+// 16 warps fill the four 16K-register sub-partitions of an SM): CTA c processes the
+// tiles c, c + grid, ... where a tile is one (b, h) and 128 query rows. 8 warps:
 //   warps 0-3  softmax + epilogue; thread t owns query row t (tensor-memory lane t)
 //   warp 4     TMA producer: Q of each tile (double-buffered) and the K/V blocks of all
 //              tiles through one ring of stages, running ahead across tile boundaries
-//   warp 5     MMA issuer (one elected lane):  S_g = Q K_g^T  (M=128, N=64, K=d, K-major operands)
-//                                       O  += P_g V_g  (M=128, N=d, K=64, P from TMEM,
-//                                                       V MN-major)
-//              It polls its barriers and issues whichever MMA is ready: PV_g as soon as
-//              P_g is written, S_{g+2} as soon as PV_g has released its buffer.
+//   warp 5     S issuer (one elected lane):  S_g = Q K_g^T  (M=128, N=64, K=d, K-major
+//              operands), once K_g has landed and PV_{g-SB} has released S/P buffer g % SB
+//   warp 7     PV issuer (one elected lane): O += P_g V_g  (M=128, N=d, K=64, P from
+//              TMEM, V MN-major), as soon as P_g is written; it releases the K/V stage
 //   warp 6     index warp: bitmap of the active positions of each tile (double-
 //              buffered) and the fused cache scatter.
 // g numbers the key blocks of a CTA across its tiles; every ring (stages, S/P buffers,
 // Q buffers, bitmaps) is indexed by g or by the tile count, and every barrier is waited
 // one phase at a time, in order, so parity waits are exact.
 //
-// Tensor memory (256 columns): two S buffers of 64 columns, each overwritten in place by
-// P as packed bf16 pairs, and O (d columns) accumulated across the blocks of a tile.
+// Tensor memory (256 columns): SB S buffers of 64 columns (three for d = 64, two for
+// d = 80), each overwritten in place by P as packed bf16 pairs, and O (d columns)
+// accumulated across the blocks of a tile. With three buffers S_{g+1} depends only on
+// PV_{g-2}, long complete, so the softmax warps run from block to block without waiting
+// for the tensor pipe.
 // Online softmax with a lazy rescale: a row keeps the max m used for its P values; a
 // block whose row max exceeds m by more than 8 (base-2 units) raises m and rescales O
 // and l by 2^(m_old - m_new); otherwise P = 2^(s - m) <= 2^8 and nothing is rescaled.
@@ -54,7 +56,7 @@ using namespace tc5;
 
 constexpr int BM = 128;          // query rows per tile
 constexpr int BN = 64;           // keys per block
-constexpr int kThreads = 224;    // 7 warps
+constexpr int kThreads = 256;    // 8 warps
 constexpr uint32_t kTmemCols = 256;
 constexpr float kRescale = 8.f;  // lazy-rescale threshold (base-2 units)
 
@@ -62,6 +64,9 @@ template <int D>
 struct Cfg {
     static constexpr int DB = D - 64;                                   // tail columns (0 or 16)
     static constexpr int kStages = (D == 64) ? 4 : 3;
+    // S/P buffers of 64 tensor-memory columns; O takes D columns after them (<= 256)
+    static constexpr int kSB = (D == 64) ? 3 : 2;
+    static_assert(64 * kSB + D <= 256, "tensor memory: S/P buffers + O exceed 256 columns");
     static constexpr uint32_t kQa = BM * 128, kQb = BM * DB * 2;        // Q tile parts
     static constexpr uint32_t kQBytes = ((kQa + kQb + 1023) / 1024) * 1024;
     static constexpr uint32_t kKa = BN * 128, kKb = BN * DB * 2;        // one K (or V) block
@@ -79,12 +84,12 @@ struct Cfg {
 enum Bar {
     Q_FULL = 0,      // [2]
     Q_EMPTY = 2,     // [2]
-    S_FULL = 4,      // [2]
-    P_FULL = 6,      // [2]
-    O_DONE = 8,      // [2] PV of block g -> O_DONE[g & 1]
-    BM_FULL = 10,    // [2]
-    BM_EMPTY = 12,   // [2]
-    KV_FULL = 14     // [S], then KV_EMPTY [S]
+    S_FULL = 4,      // [kSB <= 3]
+    P_FULL = 7,      // [kSB]
+    O_DONE = 10,     // [kSB] PV of block g -> O_DONE[g % kSB]
+    BM_FULL = 13,    // [2]
+    BM_EMPTY = 15,   // [2]
+    KV_FULL = 17     // [S], then KV_EMPTY [S]
 };
 
 template <int D>
@@ -107,6 +112,7 @@ template <int D>
 __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Params<D> P) {
     using C = Cfg<D>;
     constexpr int S = C::kStages;
+    constexpr int SB = C::kSB;
     const AttnParams &p = P.a;
     extern __shared__ unsigned char smem_raw[];
     const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
@@ -134,11 +140,13 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[Q_FULL + i], 1);
             mbar_init(&bars[Q_EMPTY + i], 1);
+            mbar_init(&bars[BM_FULL + i], 1);
+            mbar_init(&bars[BM_EMPTY + i], 4);
+        }
+        for (int i = 0; i < SB; ++i) {
             mbar_init(&bars[S_FULL + i], 1);
             mbar_init(&bars[P_FULL + i], 4);
             mbar_init(&bars[O_DONE + i], 1);
-            mbar_init(&bars[BM_FULL + i], 1);
-            mbar_init(&bars[BM_EMPTY + i], 4);
         }
         for (int i = 0; i < S; ++i) {
             mbar_init(&bars[KV_FULL + i], 1);
@@ -150,7 +158,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = *tmem_slot;
-    const uint32_t tmS0 = tm, tmO = tm + 128;
+    const uint32_t tmS0 = tm, tmO = tm + 64 * SB;
 
     if (warp == 4) {
         // ------------------------------------------------------------ producer
@@ -187,87 +195,68 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
         }
         __syncwarp();
     } else if (warp == 5) {
-        // ------------------------------------------------------------ MMA issuer
-        // The whole warp runs this loop so that every descriptor is warp-uniform; one
-        // elected lane issues each tcgen05 instruction. (Issuing from a one-lane branch
-        // costs several times more per instruction.) Lane 0's barrier tests are broadcast
-        // so that control flow stays uniform.
+        // ------------------------------------------------------------ S issuer
+        // S_g = Q K_g^T once K_g has landed, Q of its tile has landed and PV_{g-SB} has
+        // released S/P buffer g % SB. The whole warp runs the loop so that every descriptor
+        // is warp-uniform; one elected lane issues each tcgen05 instruction. Waits suspend
+        // the warp rather than poll.
         const uint32_t idS = idesc_bf16(BM, BN, 0, 0);
+        const int total = my_tiles * nblk;
+        for (int g = 0; g < total; ++g) {
+            const int it = g / nblk, j = g - it * nblk;
+            if (!mbar_wait(&bars[KV_FULL + g % S], (g / S) & 1, p.status, abort_flag)) break;
+            if (j == 0 && !mbar_wait(&bars[Q_FULL + (it & 1)], (it >> 1) & 1, p.status, abort_flag)) break;
+            if (g >= SB && !mbar_wait(&bars[O_DONE + g % SB], (g / SB - 1) & 1, p.status, abort_flag)) break;
+            tc_fence_after();
+            const unsigned char *sq = sm + C::oQ + (it & 1) * C::kQBytes;
+            const unsigned char *stg = sm + C::oStage + (g % S) * C::kStageBytes;
+            const uint64_t dQa = smem_desc(sq, 16, 1024, Swz::B128);
+            const uint64_t dKa = smem_desc(stg + C::sKa, 16, 1024, Swz::B128);
+            const uint32_t dst = tmS0 + 64 * (g % SB);
+            if (elect_one()) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma_ss(dst, desc_advance(dQa, 32 * k), desc_advance(dKa, 32 * k), idS, k > 0);
+                if constexpr (C::DB > 0)
+                    mma_ss(dst, smem_desc(sq + C::kQa, 16, 256, Swz::B32), smem_desc(stg + C::sKb, 16, 256, Swz::B32),
+                           idS, 1);
+                mma_commit(&bars[S_FULL + g % SB]);
+                if (j == nblk - 1) mma_commit(&bars[Q_EMPTY + (it & 1)]);  // Q buffer reusable
+            }
+            __syncwarp();
+        }
+        __syncwarp();
+    } else if (warp == 7) {
+        // ------------------------------------------------------------ PV issuer
+        // O += P_g V_g as soon as the softmax warps have written P_g; its commits release
+        // the S/P buffer (O_DONE) and the K/V stage. tcgen05 operations complete in issue
+        // order per issuing thread, and the S issuer orders itself after PV through O_DONE.
         const uint32_t idOa = idesc_bf16(BM, 64, 0, 1);
         const uint32_t idOb = idesc_bf16(BM, 16, 0, 1);
         const int total = my_tiles * nblk;
-        int next_s = 0, next_pv = 0;
-        uint32_t idle = 0;
-        bool ok = true;
-        while (ok && next_pv < total) {
-            bool progress = false;
-            // S_g: Q of its tile has landed, its K block has landed, and PV_{g-2} has
-            // released S/P buffer g & 1
-            if (next_s < total && next_s < next_pv + 2) {
-                const int g = next_s, it = g / nblk, j = g - it * nblk;
-                bool ready = mbar_test(&bars[KV_FULL + g % S], (g / S) & 1);
-                if (ready && g >= 2) ready = mbar_test(&bars[O_DONE + (g & 1)], ((g - 2) >> 1) & 1);
-                if (ready && j == 0) ready = mbar_test(&bars[Q_FULL + (it & 1)], (it >> 1) & 1);
-                ready = __shfl_sync(0xffffffffu, ready, 0);
-                if (ready) {
-                    tc_fence_after();
-                    const unsigned char *sq = sm + C::oQ + (it & 1) * C::kQBytes;
-                    const unsigned char *stg = sm + C::oStage + (g % S) * C::kStageBytes;
-                    const uint64_t dQa = smem_desc(sq, 16, 1024, Swz::B128);
-                    const uint64_t dKa = smem_desc(stg + C::sKa, 16, 1024, Swz::B128);
-                    const uint32_t dst = tmS0 + 64 * (g & 1);
-                    if (elect_one()) {
+        for (int g = 0; g < total; ++g) {
+            if (!mbar_wait(&bars[P_FULL + g % SB], (g / SB) & 1, p.status, abort_flag)) break;
+            // V_g landed long ago (S_g needed the same stage); waiting on its barrier phase
+            // here orders this thread's reads after the TMA write. The stage cannot have been
+            // refilled: that needs this warp's commit below.
+            if (!mbar_wait(&bars[KV_FULL + g % S], (g / S) & 1, p.status, abort_flag)) break;
+            tc_fence_after();
+            const int j = g % nblk;
+            const unsigned char *stg = sm + C::oStage + (g % S) * C::kStageBytes;
+            const uint64_t dVa = smem_desc(stg + C::sVa, 1024, 1024, Swz::B128);
+            const uint64_t dVb = smem_desc(stg + C::sVb, 256, 256, Swz::B32);
+            const uint32_t pcol = tmS0 + 64 * (g % SB);
+            if (elect_one()) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            mma_ss(dst, desc_advance(dQa, 32 * k), desc_advance(dKa, 32 * k), idS, k > 0);
-                        if constexpr (C::DB > 0)
-                            mma_ss(dst, smem_desc(sq + C::kQa, 16, 256, Swz::B32),
-                                   smem_desc(stg + C::sKb, 16, 256, Swz::B32), idS, 1);
-                        mma_commit(&bars[S_FULL + (g & 1)]);
-                        if (j == nblk - 1) mma_commit(&bars[Q_EMPTY + (it & 1)]);  // Q buffer reusable
-                    }
-                    __syncwarp();
-                    ++next_s;
-                    progress = true;
+                for (int k = 0; k < BN / 16; ++k) {
+                    const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
+                    mma_ts(tmO, pcol + 8 * k, desc_advance(dVa, 2048 * k), idOa, acc);
+                    if constexpr (C::DB > 0) mma_ts(tmO + 64, pcol + 8 * k, desc_advance(dVb, 512 * k), idOb, acc);
                 }
+                mma_commit(&bars[O_DONE + g % SB]);
+                mma_commit(&kv_empty[g % S]);
             }
-            // PV_g: P_g has been written over S_g
-            if (next_pv < next_s) {
-                const int g = next_pv, j = g % nblk;
-                const bool ready = __shfl_sync(0xffffffffu, mbar_test(&bars[P_FULL + (g & 1)], (g >> 1) & 1), 0);
-                if (ready) {
-                    tc_fence_after();
-                    const unsigned char *stg = sm + C::oStage + (g % S) * C::kStageBytes;
-                    const uint64_t dVa = smem_desc(stg + C::sVa, 1024, 1024, Swz::B128);
-                    const uint64_t dVb = smem_desc(stg + C::sVb, 256, 256, Swz::B32);
-                    const uint32_t pcol = tmS0 + 64 * (g & 1);
-                    if (elect_one()) {
-#pragma unroll
-                        for (int k = 0; k < BN / 16; ++k) {
-                            const uint32_t acc = (j > 0 || k > 0) ? 1u : 0u;
-                            mma_ts(tmO, pcol + 8 * k, desc_advance(dVa, 2048 * k), idOa, acc);
-                            if constexpr (C::DB > 0)
-                                mma_ts(tmO + 64, pcol + 8 * k, desc_advance(dVb, 512 * k), idOb, acc);
-                        }
-                        mma_commit(&bars[O_DONE + (g & 1)]);
-                        mma_commit(&kv_empty[g % S]);
-                    }
-                    __syncwarp();
-                    ++next_pv;
-                    progress = true;
-                }
-            }
-            if (progress) {
-                idle = 0;
-            } else if (*abort_flag) {
-                ok = false;
-            } else if (++idle > kSpinLimit) {
-                if (lane == 0) {
-                    report(p.status, MAR_STATUS_TIMEOUT_BIT);
-                    *abort_flag = 1;
-                }
-                ok = false;
-            }
+            __syncwarp();
         }
         __syncwarp();
     } else if (warp == 6) {
@@ -326,11 +315,11 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             const uint32_t *bm = bitmaps + (it & 1) * bm_words;
             float m_use = 0.f, l = 0.f;
             for (int j = 0; j < nblk; ++j) {
-                const int g = it * nblk + j, buf = g & 1;
+                const int g = it * nblk + j, buf = g % SB;
                 if (j == nd && nc > 0 &&
                     !(ok = mbar_wait(&bars[BM_FULL + (it & 1)], (it >> 1) & 1, p.status, abort_flag)))
                     break;
-                if (!(ok = mbar_wait(&bars[S_FULL + buf], (g >> 1) & 1, p.status, abort_flag))) break;
+                if (!(ok = mbar_wait(&bars[S_FULL + buf], (g / SB) & 1, p.status, abort_flag))) break;
                 tc_fence_after();
                 // slots of this block that are keys: dense rows below n_dense; cache rows below
                 // N whose position is not active (active positions hold stale cache rows)
@@ -366,20 +355,15 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                 if (live) {
                     float v[64];
                     tmem_ld64(lane_addr(tmS0, warp, 64 * buf), v);
-                    float mx = -INFINITY;
-                    if (valid == ~0ull) {
+                    if (valid != ~0ull) {
 #pragma unroll
-                        for (int i = 0; i < 64; ++i) {
-                            v[i] *= sl2;
-                            mx = fmaxf(mx, v[i]);
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 64; ++i) {
-                            v[i] = ((valid >> i) & 1ull) ? v[i] * sl2 : -INFINITY;
-                            mx = fmaxf(mx, v[i]);
-                        }
+                        for (int i = 0; i < 64; ++i) v[i] = ((valid >> i) & 1ull) ? v[i] : -INFINITY;
                     }
+                    // row max of the raw scores (the scale is positive), four independent chains
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) m4[i & 3] = max3f(m4[i & 3], v[2 * i], v[2 * i + 1]);
+                    const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
                     bool rescale = false;
                     float factor = 1.f;
                     if (j == 0) {
@@ -389,36 +373,33 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                         m_use = mx;
                         rescale = true;
                     }
-                    // P = 2^(s - m) as bf16 pairs over S, one half at a time
-                    float rs0 = 0.f, rs1 = 0.f;
-                    {
+                    // P = 2^(s * scale * log2(e) - m) as bf16 pairs over S, one half at a time;
+                    // one packed FMA forms both exponents of a pair
+                    const f32x2 sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_use, -m_use);
+                    f32x2 rsa = f2_pack(0.f, 0.f), rsb = rsa;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
                         uint32_t w[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float p0 = fast_exp2(v[2 * i] - m_use), p1 = fast_exp2(v[2 * i + 1] - m_use);
-                            rs0 += p0;
-                            rs1 += p1;
+                            float x0, x1;
+                            f2_unpack(f2_fma(f2_pack(v[32 * h + 2 * i], v[32 * h + 2 * i + 1]), sc2, nm2), x0, x1);
+                            const f32x2 e = f2_pack(fast_exp2(x0), fast_exp2(x1));
+                            if (i & 1) rsb = f2_add(rsb, e); else rsa = f2_add(rsa, e);
+                            float p0, p1;
+                            f2_unpack(e, p0, p1);
                             w[i] = pack_bf16x2(p0, p1);
                         }
-                        tmem_st16(lane_addr(tmS0, warp, 64 * buf), w);
+                        tmem_st16(lane_addr(tmS0, warp, 64 * buf + 16 * h), w);
                     }
-                    {
-                        uint32_t w[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float p0 = fast_exp2(v[32 + 2 * i] - m_use), p1 = fast_exp2(v[33 + 2 * i] - m_use);
-                            rs0 += p0;
-                            rs1 += p1;
-                            w[i] = pack_bf16x2(p0, p1);
-                        }
-                        tmem_st16(lane_addr(tmS0, warp, 64 * buf + 16), w);
-                    }
+                    float rs0, rs1;
+                    f2_unpack(f2_add(rsa, rsb), rs0, rs1);
                     l = l * factor + (rs0 + rs1);
                     if (__any_sync(0xffffffffu, rescale)) {
                         // O holds the tile's sum over earlier blocks; wait for PV_{g-1} and
                         // scale the rows that raised their max (the others use factor 1).
                         // PV_g, which adds this block, is issued only after P_FULL below.
-                        ok = mbar_wait(&bars[O_DONE + ((g - 1) & 1)], ((g - 1) >> 1) & 1, p.status, abort_flag);
+                        ok = mbar_wait(&bars[O_DONE + (g - 1) % SB], ((g - 1) / SB) & 1, p.status, abort_flag);
                         if (ok) {
                             tc_fence_after();
 #pragma unroll
@@ -442,10 +423,11 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                 if (!ok) break;
             }
             if (!ok) break;
-            // PV of the tile's last block was issued after PV_{g-2} finished, so its barrier
-            // phase is exact; MMAs complete in order, so it covers all of the tile's PVs.
+            // The previous phase of this barrier (PV_{gl-SB}) completed before S_gl was
+            // issued, so the parity wait is exact; MMAs complete in order, so PV_gl's
+            // completion covers all of the tile's PVs.
             const int gl = it * nblk + nblk - 1;
-            if (!(ok = mbar_wait(&bars[O_DONE + (gl & 1)], (gl >> 1) & 1, p.status, abort_flag))) break;
+            if (!(ok = mbar_wait(&bars[O_DONE + gl % SB], (gl / SB) & 1, p.status, abort_flag))) break;
             tc_fence_after();
             if (live) {
                 const int row = q0 + tid;

@@ -76,6 +76,34 @@ MAR_DEVINL float fast_exp2(float x) {
     return y;
 }
 
+// ---------------------------------------------------------------- packed fp32 pairs (sm_100+)
+// Two fp32 values in one 64-bit register pair; one instruction operates on both.
+using f32x2 = unsigned long long;
+MAR_DEVINL f32x2 f2_pack(float lo, float hi) {
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};\n" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+MAR_DEVINL void f2_unpack(f32x2 r, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;\n" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+MAR_DEVINL f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+MAR_DEVINL f32x2 f2_add(f32x2 a, f32x2 b) {
+    f32x2 r;
+    asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// max of three (sm_100+ three-input form)
+MAR_DEVINL float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // ---------------------------------------------------------------- active/cached partition
 // Builds, in shared memory, the ascending list of positions of one batch row that are
 // NOT in idx[0..A) (the cached set), using a bitmap of N bits. All threads of the

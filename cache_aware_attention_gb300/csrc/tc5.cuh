@@ -56,7 +56,10 @@ MAR_DEVINL bool mbar_test(uint64_t *bar, uint32_t parity) {
 }
 // Waits for the phase with the given parity to complete. Returns false on timeout (and
 // records it in *status); *abort (shared) is also raised so other roles can unwind.
+// try_wait costs about 200 cycles even on a phase that has already completed, so a
+// non-blocking test comes first: most waits of a well-fed pipeline find the phase done.
 MAR_DEVINL bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status, volatile int *abort) {
+    if (mbar_test(bar, parity)) return true;
     for (uint32_t i = 0; i < kSpinLimit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if (abort && *abort) return false;
