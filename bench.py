@@ -241,7 +241,7 @@ def run_mine(args, ws, rank, local):
     peaks = load_peaks()
     hbm = peaks.get("hbm_gbs", 6800.0)
     fa = brk["attn_full"]
-    roof = {"bound": "hbm", "kernel": "attn_mma_kernel<64> (full attention, N=320)",
+    roof = {"bound": "hbm", "kernel": "attn_tc5_kernel<64> (full attention, N=320)",
             "achieved": fa["gbs"], "peak": hbm, "unit": "GB/s",
             "frac": fa["gbs"] / hbm if fa["gbs"] else None, "traffic": None,
             "peak_source": "MEASURED_PEAKS.json hbm_gbs" if "hbm_gbs" in peaks else "fallback 6800 GB/s"}
@@ -276,46 +276,29 @@ def launches_per_step(t):
     return 4 if t % REFRESH_PERIOD == 0 else 7
 
 
-def breakdown(args, cfg, sets, step, mar, W, K, is_full_refresh):
-    """Average device time of each C-ABI call over K eager steps (events bracket each call)."""
-    names = ["attn_full", "attn_full+score", "topk", "gather", "cache_aware", "scatter_all", "cfg"]
-    acc = {n: [0.0, 0] for n in names}
-    pairs = []
+def breakdown(args, cfg, sets, step, mar, W, K, is_full_refresh, reps: int = 24):
+    """Device time of each C-ABI call of the step.
+
+    Each call kind is captured into one CUDA graph of ``reps`` back-to-back calls (the
+    input sets rotating, so that inputs come from HBM, not L2), replayed after one
+    warm-up replay, and timed with CUDA events on the replaying stream; the per-call
+    time is the graph's time / reps (host launch overhead excluded, the short gaps
+    between kernels of a graph included)."""
     A = cfg.A
-    nstep = min(K, 300)
-
-    def timed(name, fn):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        fn()
-        b.record()
-        pairs.append((name, a, b))
-
-    for t in range(W, W + nstep):
-        s = sets[t % N_SETS]
-        Q2, K2, V2 = s.layer2
-        Q3, K3, V3 = s.layer3
-        Kc, Vc = s.cache
-        if is_full_refresh(t):
-            timed("attn_full", lambda: mar.mar_attn_full(Q2, K2, V2, step.O2))
-            timed("attn_full", lambda: mar.mar_attn_full(Q3, K3, V3, step.O3))
-            timed("scatter_all", lambda: mar.mar_kv_scatter(K3, V3, None, Kc, Vc))
-            timed("cfg", lambda: mar.mar_cfg_residual(mar.MAR_CFG_UPDATE, s.cond, s.uncond, s.residual))
-        else:
-            act = step.active(A)
-            timed("attn_full+score", lambda: mar.mar_attn_full(Q2, K2, V2, step.O2, gen_idx=s.gen,
-                                                               score_out=step.score, workspace=step.workspace))
-            timed("topk", lambda: mar.mar_refresh_topk(step.score, s.exclude, cfg.K, out_idx=step.R,
-                                                       active_out=act))
-            qa, ka, va, oa = (step.dense(i, A) for i in range(4))
-            timed("gather", lambda: mar.mar_kv_gather([Q3, K3, V3], act, dsts=[qa, ka, va]))
-            timed("cache_aware", lambda: mar.mar_attn_cache_aware(qa, ka, va, Kc, Vc, act, O_A=oa,
-                                                                  fuse_scatter=True))
-            timed("cfg", lambda: mar.mar_cfg_residual(mar.MAR_CFG_APPLY, s.cond, s.uncond, s.residual))
-    torch.cuda.synchronize()
-    for n, a, b in pairs:
-        acc[n][0] += a.elapsed_time(b)
-        acc[n][1] += 1
+    act = step.active(A)
+    qa, ka, va, oa = (step.dense(i, A) for i in range(4))
+    calls = {
+        "attn_full": lambda s: mar.mar_attn_full(s.layer2[0], s.layer2[1], s.layer2[2], step.O2),
+        "attn_full+score": lambda s: mar.mar_attn_full(s.layer2[0], s.layer2[1], s.layer2[2], step.O2,
+                                                       gen_idx=s.gen, score_out=step.score,
+                                                       workspace=step.workspace),
+        "topk": lambda s: mar.mar_refresh_topk(step.score, s.exclude, cfg.K, out_idx=step.R, active_out=act),
+        "gather": lambda s: mar.mar_kv_gather(list(s.layer3), act, dsts=[qa, ka, va]),
+        "cache_aware": lambda s: mar.mar_attn_cache_aware(qa, ka, va, s.cache[0], s.cache[1], act, O_A=oa,
+                                                          fuse_scatter=True),
+        "scatter_all": lambda s: mar.mar_kv_scatter(s.layer3[1], s.layer3[2], None, s.cache[0], s.cache[1]),
+        "cfg": lambda s: mar.mar_cfg_residual(mar.MAR_CFG_APPLY, s.cond, s.uncond, s.residual),
+    }
     algo = {"attn_full": bytes_full_attention(cfg),
             "attn_full+score": bytes_full_attention(cfg),
             "topk": cfg.Bp * cfg.N * 4 + cfg.Bp * (cfg.G + cfg.J + cfg.K) * 4,
@@ -323,18 +306,29 @@ def breakdown(args, cfg, sets, step, mar, W, K, is_full_refresh):
             "cache_aware": bytes_cache_aware(cfg, A) + 2 * cfg.Bp * cfg.H * A * cfg.d * 2,
             "scatter_all": 4 * cfg.Bp * cfg.H * cfg.N * cfg.d * 2,
             "cfg": 3 * cfg.B * cfg.n_img * cfg.latent * 4}
+    side = torch.cuda.Stream()
     out = {}
-    for n in names:
-        tot, cnt = acc[n]
-        if cnt == 0:
-            continue
-        us = tot / cnt * 1e3
-        out[n] = {"us": us, "calls": cnt, "bytes": algo[n], "gbs": algo[n] / (us * 1e-6) / 1e9}
+    for name, fn in calls.items():
+        fn(sets[0])
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for r in range(reps):
+                fn(sets[r % N_SETS])
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        out[name] = {"us": us, "calls": reps, "bytes": algo[name], "gbs": algo[name] / (us * 1e-6) / 1e9}
+        del g
+    out["score (difference)"] = {"us": out["attn_full+score"]["us"] - out["attn_full"]["us"]}
     flops_full = 4 * cfg.Bp * cfg.H * cfg.N * cfg.N * cfg.d
-    if "attn_full" in out:
-        out["attn_full"]["tflops"] = flops_full / (out["attn_full"]["us"] * 1e-6) / 1e12
-    if "cache_aware" in out:
-        out["cache_aware"]["tflops"] = 4 * cfg.Bp * cfg.H * A * cfg.N * cfg.d / (out["cache_aware"]["us"] * 1e-6) / 1e12
+    out["attn_full"]["tflops"] = flops_full / (out["attn_full"]["us"] * 1e-6) / 1e12
+    out["cache_aware"]["tflops"] = 4 * cfg.Bp * cfg.H * A * cfg.N * cfg.d / (out["cache_aware"]["us"] * 1e-6) / 1e12
     return out
 
 
