@@ -226,6 +226,15 @@ MAR_DEVINL bool elect_one() {
     return pred != 0;
 }
 
+// Contiguous global -> shared copy by the TMA unit, completing `bytes` on `bar`. Both
+// addresses 16-byte aligned, bytes a multiple of 16.
+MAR_DEVINL void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
 }  // namespace tc5
 }  // namespace mar
 

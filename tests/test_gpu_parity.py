@@ -301,6 +301,25 @@ def test_score_and_topk(name, G, K):
     assert np.array_equal(active.cpu().numpy(), np.concatenate([excl.cpu().numpy(), R_np], 1))
 
 
+@pytest.mark.parametrize("B,H,N,d,dtype,G", [
+    (3, 1, 200, 64, torch.bfloat16, 3),      # cluster of one CTA
+    (2, 5, 333, 128, torch.bfloat16, 11),    # odd head count, two passes over the queries
+    (2, 3, 97, 80, torch.float32, 2),        # fp32 rows of 20 chunks (sequential chunk sum)
+    (2, 7, 77, 32, torch.float32, 9),
+    (2, 20, 130, 64, torch.bfloat16, 5),     # more heads than one cluster holds: two-kernel path
+])
+def test_score_shapes(B, H, N, d, dtype, G):
+    Q, Kt, V = (_rand((B, H, N, d), 520 + i, dtype) for i in range(3))
+    gen = workloads.distinct_positions(B, G, 0, N, 530).to(DEV)
+    score = torch.empty(B, N, dtype=torch.float32, device=DEV)
+    st = _status()
+    mar.mar_attn_full(Q, Kt, V, gen_idx=gen, score_out=score, status=st)
+    assert mar.mar_status_read(st) == 0
+    ref = oracle.l2_score(Q, Kt, gen)
+    rel = np.abs(score.cpu().numpy().astype(np.float64) - ref) / ref
+    assert rel.max() < 1e-6, f"score relative error {rel.max():.3g}"
+
+
 @pytest.mark.parametrize("N,E,K,levels", [(320, 8, 32, 0), (320, 8, 32, 5), (1088, 50, 64, 3), (64, 4, 4, 0),
                                           (300, 0, 300, 2), (4000, 10, 700, 0), (20, 3, 0, 0)])
 def test_topk_selection_bit_exact(N, E, K, levels):
