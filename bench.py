@@ -271,9 +271,9 @@ def run_mine(args, ws, rank, local):
 
 
 def launches_per_step(t):
-    # refresh: attn(L2) + attn(L3) + scatter + cfg = 4; cached: attn + score(2) + topk + gather +
-    # cache-aware + cfg = 7
-    return 4 if t % REFRESH_PERIOD == 0 else 7
+    # refresh: attn(L2) + attn with cache refresh (L3) + cfg = 3; cached: attn + score + topk +
+    # gather + cache-aware + cfg = 6
+    return 3 if t % REFRESH_PERIOD == 0 else 6
 
 
 def breakdown(args, cfg, sets, step, mar, W, K, is_full_refresh, reps: int = 24):
@@ -296,7 +296,8 @@ def breakdown(args, cfg, sets, step, mar, W, K, is_full_refresh, reps: int = 24)
         "gather": lambda s: mar.mar_kv_gather(list(s.layer3), act, dsts=[qa, ka, va]),
         "cache_aware": lambda s: mar.mar_attn_cache_aware(qa, ka, va, s.cache[0], s.cache[1], act, O_A=oa,
                                                           fuse_scatter=True),
-        "scatter_all": lambda s: mar.mar_kv_scatter(s.layer3[1], s.layer3[2], None, s.cache[0], s.cache[1]),
+        "attn_full_refresh": lambda s: mar.mar_attn_full_refresh(s.layer3[0], s.layer3[1], s.layer3[2], s.cache[0],
+                                                                 s.cache[1], step.O3),
         "cfg": lambda s: mar.mar_cfg_residual(mar.MAR_CFG_APPLY, s.cond, s.uncond, s.residual),
     }
     algo = {"attn_full": bytes_full_attention(cfg),
@@ -304,7 +305,7 @@ def breakdown(args, cfg, sets, step, mar, W, K, is_full_refresh, reps: int = 24)
             "topk": cfg.Bp * cfg.N * 4 + cfg.Bp * (cfg.G + cfg.J + cfg.K) * 4,
             "gather": 2 * 3 * cfg.Bp * cfg.H * A * cfg.d * 2,
             "cache_aware": bytes_cache_aware(cfg, A) + 2 * cfg.Bp * cfg.H * A * cfg.d * 2,
-            "scatter_all": 4 * cfg.Bp * cfg.H * cfg.N * cfg.d * 2,
+            "attn_full_refresh": bytes_full_attention(cfg) + 2 * cfg.Bp * cfg.H * cfg.N * cfg.d * 2,
             "cfg": 3 * cfg.B * cfg.n_img * cfg.latent * 4}
     side = torch.cuda.Stream()
     out = {}

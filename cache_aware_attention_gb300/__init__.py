@@ -68,6 +68,7 @@ def load(path: str | None = None):
         "mar_version": ([], ctypes.c_int),
         "mar_attn_full_workspace_bytes": ([SP, I32, ctypes.c_int], SZ),
         "mar_attn_full": ([SP, P, P, P, P, F, P, I32, P, P, P, SZ, P, P], ctypes.c_int),
+        "mar_attn_full_refresh": ([SP, P, P, P, P, P, P, F, P, P, P], ctypes.c_int),
         "mar_attn_cache_aware_workspace_bytes": ([SP, I32], SZ),
         "mar_attn_cache_aware": ([SP, I32, P, P, P, P, P, P, P, F, P, I32, P, SZ, P, P], ctypes.c_int),
         "mar_kv_scatter": ([SP, I32, P, P, P, P, P, P, P], ctypes.c_int),
@@ -153,6 +154,20 @@ def mar_attn_full(Q, K, V, O=None, scale: float = 0.0, gen_idx=None, score_out=N
                            _ptr(gen_idx), G, _ptr(score_out), _ptr(lse_out), _ptr(workspace), wb,
                            _ptr(status), _stream(stream))
     _check("mar_attn_full", rc)
+    return O
+
+
+def mar_attn_full_refresh(Q, K, V, K_cache, V_cache, O=None, scale: float = 0.0, lse_out=None, status=None,
+                          stream=None):
+    """Full attention of a full-refresh step plus the full cache overwrite
+    (K_cache := K, V_cache := V); one launch for bf16 with d = 64 or 80. Returns O."""
+    lib = load()
+    s = _shape(Q)
+    if O is None:
+        O = torch.empty_like(Q)
+    rc = lib.mar_attn_full_refresh(ctypes.byref(s), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(K_cache),
+                                   _ptr(V_cache), float(scale), _ptr(lse_out), _ptr(status), _stream(stream))
+    _check("mar_attn_full_refresh", rc)
     return O
 
 

@@ -113,6 +113,40 @@ int mar_attn_full(const mar_shape *s, const void *Q, const void *K, const void *
     return MAR_OK;
 }
 
+static int rows_common(const mar_shape *s, int32_t A, int n, const void *const *src, void *const *dst,
+                       const int32_t *idx, int scatter, uint32_t *d_status, mar_stream_t stream);
+
+int mar_attn_full_refresh(const mar_shape *s, const void *Q, const void *K, const void *V, void *O,
+                          void *K_cache, void *V_cache, float scale, float *lse_out, uint32_t *d_status,
+                          mar_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc != MAR_OK) return rc;
+    if (s->B == 0 || s->H == 0 || s->N == 0) return MAR_OK;
+    if (!Q || !K || !V || !O || !K_cache || !V_cache) return MAR_ERR_ARG;
+    if (K_cache == K || V_cache == V || K_cache == V_cache) return MAR_ERR_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(K_cache) ||
+        !aligned16(V_cache))
+        return MAR_ERR_ALIGN;
+    if (!aligned4(lse_out)) return MAR_ERR_ALIGN;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+    mar::AttnParams p{};
+    p.Q = Q; p.Kd = K; p.Vd = V; p.Kc = K_cache; p.Vc = V_cache; p.idx = nullptr;
+    p.O = O; p.lse = lse_out; p.status = d_status;
+    p.B = s->B; p.H = s->H; p.N = s->N; p.d = s->d;
+    p.nq = s->N; p.n_dense = s->N; p.A = 0; p.fuse_scatter = 0; p.store_kv = 1;
+    p.scale = resolve_scale(scale, s->d);
+    const bool fused = s->dtype == MAR_BF16 && mar::attn_tc5_supported(p);
+    cudaError_t e = fused ? mar::launch_attn_bf16_tc5(p, st)
+                          : (s->dtype == MAR_BF16 ? mar::launch_attn_bf16(p, st) : mar::launch_attn_f32(p, st));
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (fused) return MAR_OK;
+    // other kernels: the refresh as a second launch (a plain row copy)
+    const void *src[2] = {K, V};
+    void *dst[2] = {K_cache, V_cache};
+    return rows_common(s, s->N, 2, src, dst, nullptr, 1, d_status, stream);
+}
+
 size_t mar_attn_cache_aware_workspace_bytes(const mar_shape *s, int32_t A) {
     (void)s;
     (void)A;

@@ -11,13 +11,15 @@ namespace mar {
 //   - the dense rows Kd/Vd[bh, 0..n_dense)                (fresh K_A/V_A, or all of K/V),
 //   - followed, when idx != nullptr, by the cache rows Kc/Vc[bh, p] for every
 //     position p in [0, N) that is not in idx[b, 0..A)  (the cached set, ascending).
-// Full attention: Kd/Vd = K/V with n_dense = N, idx = nullptr.
+// Full attention: Kd/Vd = K/V with n_dense = N, idx = nullptr; with store_kv the launch
+// also copies K/V into Kc/Vc (the full cache refresh).
 // Cache-aware attention: Kd/Vd = K_A/V_A with n_dense = A, idx = active positions.
 struct AttnParams {
     const void *Q;      // [B*H, nq, d]
     const void *Kd;     // [B*H, n_dense, d]
     const void *Vd;
-    void *Kc;           // [B*H, N, d] cache (written at active rows when fuse_scatter)
+    void *Kc;           // [B*H, N, d] cache (written at active rows when fuse_scatter,
+                        // everywhere when store_kv)
     void *Vc;
     const int32_t *idx; // [B, A] active positions, or nullptr
     void *O;            // [B*H, nq, d]
@@ -26,13 +28,14 @@ struct AttnParams {
     int B, H, N, d;
     int nq, n_dense, A;
     int fuse_scatter;
+    int store_kv;       // full attention only: Kc/Vc := Kd/Vd (tcgen05 kernel only)
     float scale;        // softmax scale
 };
 
 // Launchers. Return the cudaError_t of the launch.
 cudaError_t launch_attn_f32(const AttnParams &p, cudaStream_t s);
 cudaError_t launch_attn_bf16_mma(const AttnParams &p, cudaStream_t s);
-// tcgen05/TMEM/TMA kernel (head dim 64).
+// tcgen05/TMEM/TMA kernel (head dim 64 or 80).
 bool attn_tc5_supported(const AttnParams &p);
 cudaError_t launch_attn_bf16_tc5(const AttnParams &p, cudaStream_t s);
 

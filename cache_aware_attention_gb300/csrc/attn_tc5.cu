@@ -20,7 +20,9 @@
 // tiles c, c + grid, ... where a tile is one (b, h) and 128 query rows. 8 warps:
 //   warps 0-3  softmax + epilogue; thread t owns query row t (tensor-memory lane t)
 //   warp 4     TMA producer: Q of each tile (double-buffered) and the K/V blocks of all
-//              tiles through one ring of stages, running ahead across tile boundaries
+//              tiles through one ring of stages, running ahead across tile boundaries;
+//              for full attention with the cache refresh it also stores the K/V blocks of
+//              each (b, h)'s first query tile to the cache (TMA tile stores from the stages)
 //   warp 5     S issuer (one elected lane):  S_g = Q K_g^T  (M=128, N=64, K=d, K-major
 //              operands), once K_g has landed and PV_{g-SB} has released S/P buffer g % SB
 //   warp 7     PV issuer (one elected lane): O += P_g V_g  (M=128, N=d, K=64, P from
@@ -97,10 +99,11 @@ struct Tc5Params {
     CUtensorMap mQa, mQb;    // 3-D [BH, nq, D]: box {64,128,1} (SW128) / {16,128,1} (SW32)
     CUtensorMap mKa, mKb;    // 3-D [BH, n_dense, D], box {64|16, 64, 1}: all rows / active rows
     CUtensorMap mVa, mVb;
-    CUtensorMap mKca, mKcb;  // cache-aware: 3-D [BH, N, D], box {64|16, 64, 1}
-    CUtensorMap mVca, mVcb;
+    CUtensorMap mKca, mKcb;  // cache [BH, N, D], box {64|16, 64, 1}: read (cache-aware) or
+    CUtensorMap mVca, mVcb;  // written (full attention with the cache refresh)
     AttnParams a;
     int gather;
+    int store;               // full attention: store every K/V block of query tile 0 to the cache
     int n_tiles;
 };
 
@@ -166,10 +169,31 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             tma_prefetch_desc(&P.mQa);
             tma_prefetch_desc(&P.mKa);
             tma_prefetch_desc(&P.mVa);
+            // Cache refresh (full attention, P.store): the query tile 0 of every (b, h) visits
+            // all of its key blocks, and each staged block is stored to the cache by TMA once it
+            // has landed. The store of block g is issued after the loads of block g + 1; a stage
+            // is refilled only after its store has finished reading it (bulk groups, one per
+            // block, possibly empty, so the count to wait for is fixed).
+            int pend_g = -1, pend_bh = 0, pend_row = 0;  // block whose store is due next
+            auto store_pending = [&]() -> bool {
+                if (pend_g < 0) return true;
+                const int pst = pend_g % S;
+                if (!mbar_wait(&bars[KV_FULL + pst], (pend_g / S) & 1, p.status, abort_flag)) return false;
+                const unsigned char *stg = sm + C::oStage + pst * C::kStageBytes;
+                tma_store_3d(&P.mKca, 0, pend_row, pend_bh, stg + C::sKa);
+                tma_store_3d(&P.mVca, 0, pend_row, pend_bh, stg + C::sVa);
+                if constexpr (C::DB > 0) {
+                    tma_store_3d(&P.mKcb, 64, pend_row, pend_bh, stg + C::sKb);
+                    tma_store_3d(&P.mVcb, 64, pend_row, pend_bh, stg + C::sVb);
+                }
+                pend_g = -1;
+                return true;
+            };
             bool ok = true;
             for (int it = 0; ok && it < my_tiles; ++it) {
                 const int tile = (int)blockIdx.x + it * (int)gridDim.x;
                 const int bh = tile / nqt, q0 = (tile % nqt) * BM;
+                const bool store_tile = P.store && q0 == 0;
                 const int qb = it & 1;
                 if (!(ok = mbar_wait(&bars[Q_EMPTY + qb], ((it >> 1) & 1) ^ 1, p.status, abort_flag))) break;
                 unsigned char *sq = sm + C::oQ + qb * C::kQBytes;
@@ -179,6 +203,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                 for (int j = 0; j < nblk; ++j) {
                     const int g = it * nblk + j, st = g % S;
                     if (!(ok = mbar_wait(&kv_empty[st], ((g / S) & 1) ^ 1, p.status, abort_flag))) break;
+                    if (P.store) bulk_wait_group_read<S - 2>();  // the store of block g - S is done reading
                     unsigned char *stg = sm + C::oStage + st * C::kStageBytes;
                     uint64_t *fb = &bars[KV_FULL + st];
                     mbar_arrive_expect_tx(fb, C::kKV);
@@ -190,7 +215,21 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                         tma_load_3d(stg + C::sKb, dense ? &P.mKb : &P.mKcb, 64, row, bh, fb);
                         tma_load_3d(stg + C::sVb, dense ? &P.mVb : &P.mVcb, 64, row, bh, fb);
                     }
+                    if (P.store) {
+                        if (!(ok = store_pending())) break;
+                        bulk_commit_group();
+                        if (store_tile) {
+                            pend_g = g;
+                            pend_bh = bh;
+                            pend_row = row;
+                        }
+                    }
                 }
+            }
+            if (P.store) {
+                if (ok) store_pending();
+                bulk_commit_group();
+                bulk_wait_group<0>();  // every store complete before the CTA exits
             }
         }
         __syncwarp();
@@ -495,7 +534,8 @@ cudaError_t launch(const AttnParams &p, cudaStream_t s) {
     bool ok = map3<D>(&P.mQa, p.Q, p.nq, bh, 64, BM) && map3<D>(&P.mQb, p.Q, p.nq, bh, tw, BM);
     ok = ok && map3<D>(&P.mKa, p.Kd, p.n_dense, bh, 64, BN) && map3<D>(&P.mKb, p.Kd, p.n_dense, bh, tw, BN);
     ok = ok && map3<D>(&P.mVa, p.Vd, p.n_dense, bh, 64, BN) && map3<D>(&P.mVb, p.Vd, p.n_dense, bh, tw, BN);
-    if (P.gather) {
+    P.store = (!P.gather && p.store_kv) ? 1 : 0;
+    if (P.gather || P.store) {
         ok = ok && map3<D>(&P.mKca, p.Kc, p.N, bh, 64, BN) && map3<D>(&P.mKcb, p.Kc, p.N, bh, tw, BN);
         ok = ok && map3<D>(&P.mVca, p.Vc, p.N, bh, 64, BN) && map3<D>(&P.mVcb, p.Vc, p.N, bh, tw, BN);
     } else {

@@ -226,6 +226,23 @@ MAR_DEVINL bool elect_one() {
     return pred != 0;
 }
 
+// Tile store shared -> global by the TMA unit (bulk-group completion). Rows or columns of
+// the box outside the tensor are not written.
+MAR_DEVINL void tma_store_3d(const CUtensorMap *m, int c0, int c1, int c2, const void *src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
+                 : "memory");
+}
+MAR_DEVINL void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// Waits until at most N committed bulk groups of this thread still read shared memory.
+template <int N> MAR_DEVINL void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;\n" ::"n"(N) : "memory");
+}
+// Waits until at most N committed bulk groups of this thread are incomplete.
+template <int N> MAR_DEVINL void bulk_wait_group() {
+    asm volatile("cp.async.bulk.wait_group %0;\n" ::"n"(N) : "memory");
+}
 // Contiguous global -> shared copy by the TMA unit, completing `bytes` on `bar`. Both
 // addresses 16-byte aligned, bytes a multiple of 16.
 MAR_DEVINL void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {

@@ -17,8 +17,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (mar_attn_cache_aware, mar_attn_full, mar_attn_full_workspace_bytes, mar_kv_gather,
-               mar_kv_scatter, mar_refresh_topk)
+from . import (mar_attn_cache_aware, mar_attn_full, mar_attn_full_refresh, mar_attn_full_workspace_bytes,
+               mar_kv_gather, mar_refresh_topk)
 
 REFRESH_PERIOD = 3
 
@@ -70,8 +70,8 @@ class DecodeStep:
         Kc, Vc = cache
         if is_full_refresh(step):
             mar_attn_full(Q2, K2, V2, self.O2, status=self.status, stream=stream)
-            mar_attn_full(Q3, K3, V3, self.O3, status=self.status, stream=stream)
-            mar_kv_scatter(K3, V3, None, Kc, Vc, status=self.status, stream=stream)
+            # layer 3: full attention and the whole-cache overwrite in one call
+            mar_attn_full_refresh(Q3, K3, V3, Kc, Vc, self.O3, status=self.status, stream=stream)
             return ("full", self.O3)
         A = exclude.shape[1] + self.K
         act = self.active(A)

@@ -99,8 +99,9 @@ int mar_version(void);
  * [M] Key Design 1: the weights from the G generating queries to every token,
  * averaged over heads (and over the generating queries):
  *   score[b,j] = 1/(H*G) * sum_h sum_g softmax_j(scale * <Q[b,h,gen[b,g],:], K[b,h,j,:]>)
- * The score is evaluated to about 1e-7 relative (fp32 products, fp64 sums) so
- * that the top-K built on it matches an exact evaluation except on near-ties.
+ * The score is evaluated to about 1e-7 relative (fp32 products, sums carried to
+ * fp64-grade accuracy) so that the top-K built on it matches an exact evaluation
+ * except on near-ties.
  *
  *  Q, K, V, O  [B,H,N,d] (dtype); O may not alias Q, K or V.
  *  scale       softmax scale; 0 selects 1/sqrt(d).
@@ -116,6 +117,29 @@ int mar_attn_full(const mar_shape *shape, const void *Q, const void *K, const vo
                   void *O, float scale, const int32_t *gen_idx, int32_t G,
                   float *score_out, float *lse_out, void *workspace,
                   size_t workspace_bytes, uint32_t *d_status, mar_stream_t stream);
+
+/*
+ * mar_attn_full_refresh -- full attention of a full-refresh step together with the
+ * full cache overwrite of that layer.
+ *
+ * [M] Key Design 3: on a full-refresh step every token is recomputed at every
+ * layer and the layer's cache is rebuilt from the fresh K/V (Key Design 2 keeps
+ * the latest projection of every token). This call computes exactly the O (and
+ * lse) of mar_attn_full for Q, K, V and leaves
+ *   K_cache[b,h,j,:] = K[b,h,j,:],  V_cache[b,h,j,:] = V[b,h,j,:]   for all j
+ * (bit copies), i.e. mar_attn_full followed by mar_kv_scatter with active_idx ==
+ * NULL. For bf16 with d = 64 or 80 both happen in one launch: the attention kernel
+ * stores the K/V tiles it has staged in shared memory, so K and V are read from
+ * memory once; other shapes take two launches.
+ *
+ *  Q, K, V, O        [B,H,N,d] (dtype); O may not alias Q, K or V.
+ *  K_cache, V_cache  [B,H,N,d] (dtype), overwritten; must not alias Q, K, V, O or
+ *                    each other.
+ *  scale, lse_out    as for mar_attn_full.
+ */
+int mar_attn_full_refresh(const mar_shape *shape, const void *Q, const void *K, const void *V,
+                          void *O, void *K_cache, void *V_cache, float scale, float *lse_out,
+                          uint32_t *d_status, mar_stream_t stream);
 
 /*
  * mar_attn_full_noalloc -- mar_attn_full for callers that cannot allocate.

@@ -111,3 +111,14 @@ def test_binding_rejects_cpu_tensors(lib):
     x = torch.zeros(1, 1, 8, 32, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         mar.mar_attn_full(x, x, x)
+
+
+def test_attn_full_refresh_validation(lib):
+    def call(shape, q=FAKE, k=FAKE + 256, v=FAKE + 512, o=FAKE + 768, kc=FAKE + 1024, vc=FAKE + 1280, lse=None):
+        return lib.mar_attn_full_refresh(shape, q, k, v, o, kc, vc, 0.0, lse, None, None)
+    assert call(_shape(d=48)) == -2                 # unsupported head dim
+    assert call(_shape(), kc=None) == -1            # NULL cache
+    assert call(_shape(), kc=FAKE + 256) == -1      # K cache aliases K
+    assert call(_shape(), vc=FAKE + 1024) == -1     # V cache aliases K cache
+    assert call(_shape(), vc=FAKE + 1288) == -4     # misaligned cache
+    assert call(_shape(B=0)) == 0                   # empty: no-op

@@ -84,6 +84,41 @@ def test_full_attention_config_sampled_rows(name):
         P.assert_close(O[b:b + 1], O_ref, "bf16", f"{name} row {b}")
 
 
+# ------------------------------------------------------------------------------ full attention + cache refresh
+@pytest.mark.parametrize("dtype,B,H,N,d", [
+    ("bf16", 4, 12, 320, 64),     # MAR-B head shape, one launch
+    ("bf16", 2, 16, 320, 80),     # d = 80: tail tiles stored too
+    ("bf16", 3, 2, 200, 64),      # ragged last key block: the store is clipped at N
+    ("bf16", 2, 3, 50, 64),       # fewer keys than one block
+    ("bf16", 1, 4, 1088, 80),     # several query tiles per (b, h): only tile 0 stores
+    ("bf16", 2, 2, 77, 128),      # two-launch path (mma.sync kernel + row copy)
+    ("f32", 2, 2, 130, 32),       # two-launch path (fp32 kernel + row copy)
+])
+def test_full_attention_refresh(dtype, B, H, N, d):
+    t = DT[dtype]
+    Q, K, V = (_rand((B, H, N, d), 40 + i, t) for i in range(3))
+    Kc = torch.full((B, H, N, d), float("nan"), dtype=t, device=DEV)
+    Vc = torch.full((B, H, N, d), float("nan"), dtype=t, device=DEV)
+    lse = torch.empty(B, H, N, dtype=torch.float32, device=DEV)
+    st = _status()
+    O = mar.mar_attn_full_refresh(Q, K, V, Kc, Vc, lse_out=lse, status=st)
+    torch.cuda.synchronize()
+    assert mar.mar_status_read(st) == 0
+    assert np.array_equal(P.bits(Kc), P.bits(K)) and np.array_equal(P.bits(Vc), P.bits(V))
+    rows = range(B) if B * H * N <= 20000 else [0, B - 1]
+    for b in rows:
+        O_ref, L_ref = oracle.full_attn(Q[b:b + 1], K[b:b + 1], V[b:b + 1])
+        P.assert_close(O[b:b + 1], O_ref, dtype, f"O row {b}")
+        np.testing.assert_allclose(lse[b:b + 1].cpu().numpy(), L_ref, atol=1e-5 if dtype == "f32" else 2e-4, rtol=0)
+
+
+def test_full_attention_refresh_rejects_aliasing():
+    Q, K, V = (_rand((1, 2, 64, 64), 50 + i, torch.bfloat16) for i in range(3))
+    with pytest.raises(mar.MarError) as e:
+        mar.mar_attn_full_refresh(Q, K, V, K, torch.empty_like(V))
+    assert e.value.code == -1  # MAR_ERR_ARG
+
+
 # ------------------------------------------------------------------------------ cache-aware attention
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("B,H,N,A,d", [(1, 2, 64, 8, 32), (2, 3, 300, 70, 64), (2, 2, 320, 40, 80),
