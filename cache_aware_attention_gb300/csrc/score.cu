@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(256) score_reduce_kernel(ScoreParams p) {
 }
 
 // ------------------------------------------------------------------------ cluster kernel
-constexpr int kCThreads = 256;
+constexpr int kCThreads = 128;   // 4 warps: with <= 80 registers and ~33 KB, 6 CTAs per SM
 constexpr int kCWarps = kCThreads / 32;
 constexpr int kMaxCluster = 16;
 constexpr int kQReg = 4;                // generating queries per pass (held in registers)
@@ -226,7 +226,7 @@ MAR_DEVINL void load_chunk(const T *src, float (&v)[16 / sizeof(T)]) {
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kCThreads, 4) score_cluster_kernel(ScoreParams p, int krows) {
+__global__ void __launch_bounds__(kCThreads, 6) score_cluster_kernel(ScoreParams p, int krows) {
     namespace cg = cooperative_groups;
     using namespace tc5;
     cg::cluster_group cluster = cg::this_cluster();

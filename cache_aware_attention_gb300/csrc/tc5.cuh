@@ -24,14 +24,12 @@ MAR_DEVINL void mbar_init(uint64_t *bar, uint32_t count) {
 }
 MAR_DEVINL void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;\n" ::); }
 
+// The arrival's state token goes to the sink: no register waits on the arrive's latency.
 MAR_DEVINL void mbar_arrive(uint64_t *bar) {
-    asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(smem_u32(bar))
-                 : "memory");
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
 }
 MAR_DEVINL void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}\n" ::"r"(
-                     smem_u32(bar)),
-                 "r"(bytes)
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
 }
 MAR_DEVINL bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
