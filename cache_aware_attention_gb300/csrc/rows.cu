@@ -14,34 +14,42 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// blockIdx.x and the thread index cover one batch row's (tensor, row, chunk) 16-byte
+// vectors, neighbouring threads moving neighbouring chunks of a row; blockIdx.y steps over
+// the batch rows. A thread reads its row's position once and copies that chunk for every
+// head, the head loop unrolled so that its loads are in flight together. 32-bit index
+// arithmetic only.
 __global__ void __launch_bounds__(kThreads) rows_kernel(RowCopyParams p) {
     const int vec = p.row_bytes >> 4;
-    const int64_t per_tensor = (int64_t)p.B * p.H * p.A * vec;
-    const int64_t total = per_tensor * p.n_tensors;
-    for (int64_t t = (int64_t)blockIdx.x * kThreads + threadIdx.x; t < total;
-         t += (int64_t)gridDim.x * kThreads) {
-        const int tensor = (int)(t / per_tensor);
-        int64_t r = t - tensor * per_tensor;
-        const int c = (int)(r % vec);
-        r /= vec;
-        const int a = (int)(r % p.A);
-        const int64_t bh = r / p.A;
-        const int b = (int)(bh / p.H);
+    const int av = p.A * vec;
+    const int i = (int)blockIdx.x * kThreads + (int)threadIdx.x;
+    if (i >= av * p.n_tensors) return;
+    const int tensor = i / av;
+    const int r = i - tensor * av;
+    const int a = r / vec, c = r - a * vec;
+    const char *src_base = static_cast<const char *>(p.src[tensor]);
+    char *dst_base = static_cast<char *>(p.dst[tensor]);
+    for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
         int pos = a;
         if (p.idx) {
             pos = p.idx[(int64_t)b * p.A + a];
             if (pos < 0 || pos >= p.N) {
-                if (tensor == 0 && c == 0 && (bh % p.H) == 0) report(p.status, MAR_STATUS_INDEX_RANGE);
+                if (tensor == 0 && c == 0) report(p.status, MAR_STATUS_INDEX_RANGE);
                 continue;
             }
         }
-        const int64_t dense_row = bh * p.A + a, full_row = bh * p.N + pos;
-        const int64_t src_row = p.scatter ? dense_row : full_row;
-        const int64_t dst_row = p.scatter ? full_row : dense_row;
-        const uint4 *src = reinterpret_cast<const uint4 *>(
-            static_cast<const char *>(p.src[tensor]) + src_row * p.row_bytes);
-        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<char *>(p.dst[tensor]) + dst_row * p.row_bytes);
-        dst[c] = src[c];
+        const int64_t bh0 = (int64_t)b * p.H;
+        const int64_t dense0 = bh0 * p.A + a, full0 = bh0 * p.N + pos;
+        const int64_t src0 = p.scatter ? dense0 : full0, dst0 = p.scatter ? full0 : dense0;
+        const int64_t src_step = (int64_t)(p.scatter ? p.A : p.N) * p.row_bytes;
+        const int64_t dst_step = (int64_t)(p.scatter ? p.N : p.A) * p.row_bytes;
+        const char *sp = src_base + src0 * p.row_bytes + 16 * c;
+        char *dp = dst_base + dst0 * p.row_bytes + 16 * c;
+#pragma unroll 4
+        for (int h = 0; h < p.H; ++h) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(sp + h * src_step);
+            *reinterpret_cast<uint4 *>(dp + h * dst_step) = v;
+        }
     }
 }
 
@@ -95,9 +103,12 @@ int grid_for(int64_t work) {
 }  // namespace
 
 cudaError_t launch_rows(const RowCopyParams &p, cudaStream_t s) {
-    const int64_t total = (int64_t)p.B * p.H * p.A * (p.row_bytes / 16) * p.n_tensors;
-    if (total == 0) return cudaSuccess;
-    rows_kernel<<<grid_for(total), kThreads, 0, s>>>(p);
+    const int64_t per_bh = (int64_t)p.A * (p.row_bytes / 16) * p.n_tensors;
+    if (per_bh == 0 || p.B == 0 || p.H == 0) return cudaSuccess;
+    if (per_bh > 0x7fffffffLL - kThreads) return cudaErrorInvalidValue;
+    const unsigned gx = (unsigned)((per_bh + kThreads - 1) / kThreads);
+    const unsigned gy = (unsigned)(p.B < 65535 ? p.B : 65535);
+    rows_kernel<<<dim3(gx, gy), kThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 
