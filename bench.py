@@ -46,6 +46,10 @@ UNIT = "tok/s"
 CONFIG = "mar_b"
 N_SETS = 3
 REFRESH_PERIOD = 3
+# DRAM bytes (read + write) of one full-attention launch on this workload, from the ncu
+# capture summarised in profiles/attn_tc5_full_mar_b.md (dram__bytes_read.sum +
+# dram__bytes_write.sum); None once the kernel has changed since that capture.
+FULL_ATTN_DRAM_BYTES = 94.4576e6 + 8.120832e6
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -243,8 +247,13 @@ def run_mine(args, ws, rank, local):
     fa = brk["attn_full"]
     roof = {"bound": "hbm", "kernel": "attn_tc5_kernel<64> (full attention, N=320)",
             "achieved": fa["gbs"], "peak": hbm, "unit": "GB/s",
-            "frac": fa["gbs"] / hbm if fa["gbs"] else None, "traffic": None,
+            "frac": fa["gbs"] / hbm if fa["gbs"] else None, "traffic": FULL_ATTN_DRAM_BYTES,
+            "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch "
+                              "(profiles/attn_tc5_full_mar_b.md)",
             "peak_source": "MEASURED_PEAKS.json hbm_gbs" if "hbm_gbs" in peaks else "fallback 6800 GB/s"}
+    ca = brk["cache_aware"]
+    roof_ca = {"bound": "hbm", "kernel": "attn_tc5_kernel<64> (cache-aware attention + fused scatter, A=40)",
+               "achieved": ca["gbs"], "peak": hbm, "unit": "GB/s", "frac": ca["gbs"] / hbm if ca["gbs"] else None}
     cpu = cpu_baseline(cfg, budget_s=args.cpu_seconds) if (rank == 0 and ws == 1 and not args.no_cpu) else None
     n_launch = sum(launches_per_step(t) for t in range(W, W + K))
     line = {
@@ -260,6 +269,7 @@ def run_mine(args, ws, rank, local):
                    "l2": f"{N_SETS} rotating input sets (~{N_SETS * 8 * bytes_full_attention(cfg) // 4 // 2**20} MB "
                          "total, > L2), no flush", "timing": "CUDA graph replay, events on the stream"},
         "roofline": roof,
+        "roofline_cache_aware": roof_ca,
         "breakdown": brk,
         "e2e": e2e,
         "gpu_launches": n_launch,
