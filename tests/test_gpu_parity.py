@@ -342,6 +342,9 @@ def test_score_and_topk(name, G, K):
     (2, 3, 97, 80, torch.float32, 2),        # fp32 rows of 20 chunks (sequential chunk sum)
     (2, 7, 77, 32, torch.float32, 9),
     (2, 20, 130, 64, torch.bfloat16, 5),     # more heads than one cluster holds: two-kernel path
+    (2, 3, 333, 64, torch.bfloat16, 4),      # ragged N
+    (1, 2, 64, 64, torch.bfloat16, 1),
+    (2, 12, 640, 64, torch.bfloat16, 4),
 ])
 def test_score_shapes(B, H, N, d, dtype, G):
     Q, Kt, V = (_rand((B, H, N, d), 520 + i, dtype) for i in range(3))
@@ -353,6 +356,26 @@ def test_score_shapes(B, H, N, d, dtype, G):
     ref = oracle.l2_score(Q, Kt, gen)
     rel = np.abs(score.cpu().numpy().astype(np.float64) - ref) / ref
     assert rel.max() < 1e-6, f"score relative error {rel.max():.3g}"
+
+
+@pytest.mark.parametrize("G,d", [(3, 64), (3, 80)])
+def test_score_reports_bad_generating_position(G, d):
+    # an out-of-range generating position is reported and left out of the score
+    B, H, N = 2, 4, 150
+    Q, Kt, V = (_rand((B, H, N, d), 540 + i, torch.bfloat16) for i in range(3))
+    gen = workloads.distinct_positions(B, G, 0, N, 541).to(DEV)
+    gen[1, 2] = N + 5
+    score = torch.empty(B, N, dtype=torch.float32, device=DEV)
+    st = _status()
+    mar.mar_attn_full(Q, Kt, V, gen_idx=gen, score_out=score, status=st)
+    assert mar.mar_status_read(st) & mar.MAR_STATUS_INDEX_RANGE
+    ref0 = oracle.l2_score(Q[:1], Kt[:1], gen[:1])
+    rel = np.abs(score[:1].cpu().numpy().astype(np.float64) - ref0) / ref0
+    assert rel.max() < 1e-6
+    # row 1: the valid generating queries only, averaged over H * G (the invalid one adds 0)
+    ref1 = oracle.l2_score(Q[1:], Kt[1:], gen[1:, :2]) * (2.0 / G)
+    rel1 = np.abs(score[1:].cpu().numpy().astype(np.float64) - ref1) / ref1
+    assert rel1.max() < 1e-6
 
 
 @pytest.mark.parametrize("N,E,K,levels", [(320, 8, 32, 0), (320, 8, 32, 5), (1088, 50, 64, 3), (64, 4, 4, 0),
