@@ -15,6 +15,10 @@ Parity status of each function (pins live in ``tests/test_oracle_pins.py``):
   l2_score           pinned: row sums = 1, head linearity, single-query softmax
   topk               pinned: numpy lexsort, brute-force subset search, ties
   cfg                pinned: closed-form identities, exact fp32 subtraction
+  token_cosine       pinned: scipy's cosine distance, closed forms (x vs x, -x, 2x,
+                     orthogonal), a hand-derived case, zero-vector conventions
+  select_recompute   pinned: threshold edge cases (equal to tau, NaN), forced tokens
+  topk_pairs         pinned: pair symmetry, numpy lexsort of the fp32 summed scores
 """
 from __future__ import annotations
 
@@ -69,6 +73,10 @@ def _load():
             lib.oracle_topk.argtypes = [I, I, P, I, P, I, P]
             lib.oracle_topk.restype = ctypes.c_int
             lib.oracle_cfg.argtypes = [ctypes.c_int, I, P, P, P, D, P, P, P]
+            lib.oracle_token_cosine.argtypes = [I, I, I, I, P, P, P]
+            lib.oracle_token_cosine.restype = None
+            lib.oracle_select_recompute.argtypes = [I, I, P, ctypes.c_float, P, I, P, P]
+            lib.oracle_select_recompute.restype = ctypes.c_int
             lib.oracle_cfg.restype = None
             _lib = lib
     return _lib
@@ -207,3 +215,41 @@ def cfg(mode: int, cond, uncond=None, residual=None, w: float | None = None):
                        _ptr(ro) if ro is not None else None,
                        _ptr(go) if go is not None else None)
     return uo, ro, go
+
+
+def token_cosine(X, Y) -> np.ndarray:
+    """Per-token cosine similarity [B, N] (fp64) of two [B, H, N, d] feature tensors,
+    a token's feature being its values over all heads."""
+    x, y = _f32(X), _f32(Y)
+    B, H, N, d = x.shape
+    out = np.empty((B, N), np.float64)
+    _load().oracle_token_cosine(B, H, N, d, _ptr(x), _ptr(y), _ptr(out))
+    return out
+
+
+def select_recompute(cos, tau: float, force=None):
+    """Token-cache recompute set from fp32 similarities [B, N]: positions with not
+    (cos > tau), or forced; returns (idx [B, N] ascending then -1, count [B])."""
+    c = _f32(cos)
+    B, N = c.shape
+    f = _i32(force).reshape(B, -1) if force is not None else np.zeros((B, 0), np.int32)
+    F = f.shape[1]
+    idx = np.empty((B, N), np.int32)
+    cnt = np.empty(B, np.int32)
+    if _load().oracle_select_recompute(B, N, _ptr(c), np.float32(tau), _ptr(f) if F else None, F,
+                                       _ptr(idx), _ptr(cnt)) != 0:
+        raise ValueError("forced position out of range")
+    return idx, cnt
+
+
+def topk_pairs(score, exclude, K: int) -> np.ndarray:
+    """Shared refresh set of classifier-free-guidance pairs: rows b and b + B/2 take the
+    top-K of the fp32 sum of their scores (an IEEE single addition, as on the GPU), with
+    row b's exclusions; returns [B, K] with both rows of a pair equal."""
+    sc = _f32(score)
+    B2, N = sc.shape
+    Bp = B2 // 2
+    comb = (sc[:Bp] + sc[Bp:]).astype(np.float32)      # float32 + float32 in float32
+    ex = _i32(exclude).reshape(B2, -1)
+    R = topk(comb.astype(np.float64), ex[:Bp], K)
+    return np.concatenate([R, R], 0)

@@ -411,3 +411,76 @@ void oracle_cfg(int mode, int64_t n, const float *cond, const float *uncond_in,
         if (guided) guided[i] = u + w * (c - u);
     }
 }
+
+/* ------------------------------------------------------------------------- */
+/* Token similarity between two decode steps.                                */
+/*                                                                           */
+/* [L] Token Cache: in the deeper layers a token whose current feature is    */
+/* close, in cosine similarity, to its cached feature reuses the cached      */
+/* value. [M] Figure 1 / Figures 10-11: the same cosine between the key      */
+/* (value) projections of consecutive steps shows which tokens drift.       */
+/* A token's feature is the concatenation over the heads: for layout         */
+/* [B, H, N, d], token (b, n) has the H*d values X[b, h, n, :] for all h.   */
+/*   cos = <x, y> / (|x| |y|);  both zero -> 1, one zero -> 0.               */
+/* X, Y [B, H, N, d] float (bf16 inputs widened exactly), out [B, N].       */
+/* ------------------------------------------------------------------------- */
+void oracle_token_cosine(int64_t B, int64_t H, int64_t N, int64_t d, const float *X,
+                         const float *Y, double *out)
+{
+    #pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t n = 0; n < N; ++n) {
+            double xy = 0.0, xx = 0.0, yy = 0.0;
+            for (int64_t h = 0; h < H; ++h) {
+                const float *x = X + ((b * H + h) * N + n) * d;
+                const float *y = Y + ((b * H + h) * N + n) * d;
+                for (int64_t i = 0; i < d; ++i) {
+                    xy += (double)x[i] * (double)y[i];
+                    xx += (double)x[i] * (double)x[i];
+                    yy += (double)y[i] * (double)y[i];
+                }
+            }
+            double c;
+            if (xx == 0.0 && yy == 0.0) c = 1.0;
+            else if (xx == 0.0 || yy == 0.0) c = 0.0;
+            else c = xy / (sqrt(xx) * sqrt(yy));
+            out[b * N + n] = c;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Token-cache recompute set.                                                */
+/*                                                                           */
+/* [L] Token Cache: tokens whose similarity to the cached feature is high   */
+/* reuse the cached value; the others are recomputed. Here a token is       */
+/* recomputed unless cos > tau (so a NaN similarity is recomputed), or when  */
+/* it is in the forced set (e.g. the tokens decoded at this step). The       */
+/* decision is taken on the given fp32 similarities.                         */
+/* cos [B, N] float, force [B, F] (F may be 0), out_idx [B, N]: the          */
+/* recomputed positions ascending, then -1; out_count [B].                   */
+/* Returns -1 when a forced position is out of range (it is ignored).        */
+/* ------------------------------------------------------------------------- */
+int oracle_select_recompute(int64_t B, int64_t N, const float *cosv, float tau,
+                            const int32_t *force, int64_t F, int32_t *out_idx,
+                            int32_t *out_count)
+{
+    int bad = 0;
+    for (int64_t b = 0; b < B; ++b) {
+        unsigned char *f = (unsigned char *)calloc((size_t)(N > 0 ? N : 1), 1);
+        for (int64_t k = 0; k < F; ++k) {
+            int32_t p = force[b * F + k];
+            if (p < 0 || p >= N) { bad = 1; continue; }
+            f[p] = 1;
+        }
+        int32_t cnt = 0;
+        for (int64_t n = 0; n < N; ++n) {
+            const float c = cosv[b * N + n];
+            if (f[n] || !(c > tau)) out_idx[b * N + cnt++] = (int32_t)n;
+        }
+        for (int64_t n = cnt; n < N; ++n) out_idx[b * N + n] = -1;
+        out_count[b] = cnt;
+        free(f);
+    }
+    return bad ? -1 : 0;
+}

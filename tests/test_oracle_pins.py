@@ -351,3 +351,79 @@ def test_cfg_apply_is_exact_fp32_subtraction_and_round_trips(oracle_lib):
     np.testing.assert_allclose(g1, cond, atol=1e-12)
     _, _, g0 = oracle.cfg(oracle.CFG_APPLY, cond, residual=res, w=0.0)
     np.testing.assert_array_equal(g0, u)
+
+
+# ------------------------------------------------------------------------------ token similarity
+def test_token_cosine_matches_scipy_on_the_concatenated_heads(oracle_lib):
+    from scipy.spatial import distance
+    B, H, N, d = 2, 3, 7, 8
+    X, Y = _rand((B, H, N, d), 901).numpy(), _rand((B, H, N, d), 902).numpy()
+    got = oracle.token_cosine(X, Y)
+    for b in range(B):
+        for n in range(N):
+            x = X[b, :, n, :].astype(np.float64).reshape(-1)      # the token's H*d features
+            y = Y[b, :, n, :].astype(np.float64).reshape(-1)
+            assert got[b, n] == pytest.approx(1.0 - distance.cosine(x, y), abs=1e-12)
+
+
+def test_token_cosine_closed_forms(oracle_lib):
+    X = _rand((1, 2, 4, 16), 903).numpy()
+    np.testing.assert_allclose(oracle.token_cosine(X, X), 1.0, atol=1e-12)
+    np.testing.assert_allclose(oracle.token_cosine(X, -X), -1.0, atol=1e-12)
+    np.testing.assert_allclose(oracle.token_cosine(X, 2.5 * X), 1.0, atol=1e-12)   # scale invariant
+    # orthogonal: x in the first head only, y in the second head only
+    x = np.zeros((1, 2, 1, 4), np.float32)
+    y = np.zeros((1, 2, 1, 4), np.float32)
+    x[0, 0, 0, :] = [1, 2, 3, 4]
+    y[0, 1, 0, :] = [4, 3, 2, 1]
+    assert oracle.token_cosine(x, y)[0, 0] == 0.0
+    # hand-derived: x = (1, 0 | 0, 0), y = (1, 1 | 0, 0) -> 1 / sqrt(2)
+    x = np.zeros((1, 2, 1, 2), np.float32)
+    y = np.zeros((1, 2, 1, 2), np.float32)
+    x[0, 0, 0] = [1, 0]
+    y[0, 0, 0] = [1, 1]
+    assert oracle.token_cosine(x, y)[0, 0] == pytest.approx(1 / math.sqrt(2), abs=1e-15)
+    # a component in the second head counts: x = (1, 0 | 1, 0), y = (1, 0 | 0, 0) -> 1/sqrt(2)
+    x[0, 1, 0] = [1, 0]
+    y[0, 0, 0] = [1, 0]
+    assert oracle.token_cosine(x, y)[0, 0] == pytest.approx(1 / math.sqrt(2), abs=1e-15)
+
+
+def test_token_cosine_zero_vectors(oracle_lib):
+    z = np.zeros((1, 1, 2, 4), np.float32)
+    x = np.ones((1, 1, 2, 4), np.float32)
+    np.testing.assert_array_equal(oracle.token_cosine(z, z), 1.0)
+    np.testing.assert_array_equal(oracle.token_cosine(z, x), 0.0)
+    np.testing.assert_array_equal(oracle.token_cosine(x, z), 0.0)
+
+
+def test_select_recompute_threshold_edges(oracle_lib):
+    cos = np.array([[0.5, 0.99, 0.9, np.nan, 0.95, -1.0],
+                    [1.0, 1.0, 1.0, 1.0, 1.0, 1.0]], np.float32)
+    idx, cnt = oracle.select_recompute(cos, 0.9)
+    assert cnt.tolist() == [4, 0]
+    assert idx[0].tolist() == [0, 2, 3, 5, -1, -1]      # equal to tau and NaN are recomputed
+    assert idx[1].tolist() == [-1] * 6
+    idx, cnt = oracle.select_recompute(cos, 0.9, force=np.array([[1, 4], [5, 0]], np.int32))
+    assert idx[0].tolist() == [0, 1, 2, 3, 4, 5] and cnt[0] == 6
+    assert idx[1].tolist() == [0, 5, -1, -1, -1, -1] and cnt[1] == 2   # ascending, whatever the force order
+    with pytest.raises(ValueError):
+        oracle.select_recompute(cos, 0.9, force=np.array([[7], [0]], np.int32))
+
+
+def test_topk_pairs_symmetry_and_lexsort(oracle_lib):
+    g = np.random.default_rng(905)
+    Bp, N, E, K = 3, 40, 5, 7
+    sc = g.random((2 * Bp, N)).astype(np.float32)
+    sc[:, 3] = sc[:, 4]                                  # exact ties inside a pair's sum
+    ex = np.stack([g.permutation(N)[:E] for _ in range(Bp)]).astype(np.int32)
+    ex = np.concatenate([ex, ex], 0)
+    R = oracle.topk_pairs(sc, ex, K)
+    np.testing.assert_array_equal(R[:Bp], R[Bp:])
+    swapped = np.concatenate([sc[Bp:], sc[:Bp]], 0)       # cond and uncond exchanged
+    np.testing.assert_array_equal(oracle.topk_pairs(swapped, ex, K), R)
+    for b in range(Bp):
+        comb = (sc[b] + sc[b + Bp]).astype(np.float32).astype(np.float64)
+        cand = np.setdiff1d(np.arange(N), ex[b])
+        order = np.lexsort((cand, -comb[cand]))         # score descending, position ascending
+        np.testing.assert_array_equal(R[b], np.sort(cand[order[:K]]))
