@@ -74,6 +74,9 @@ def load(path: str | None = None):
         "mar_kv_scatter": ([SP, I32, P, P, P, P, P, P, P], ctypes.c_int),
         "mar_kv_gather": ([SP, I32, I32, P, P, P, P, P], ctypes.c_int),
         "mar_refresh_topk": ([I32, I32, P, P, I32, I32, P, P, P, P], ctypes.c_int),
+        "mar_refresh_topk_pairs": ([I32, I32, P, P, I32, I32, P, P, P, P], ctypes.c_int),
+        "mar_token_cosine": ([SP, P, P, P, P], ctypes.c_int),
+        "mar_select_recompute": ([I32, I32, P, F, P, I32, P, P, P, P], ctypes.c_int),
         "mar_cfg_residual": ([I32, I64, P, P, P, F, P, P], ctypes.c_int),
         "mar_status_read": ([P, P, P], ctypes.c_int),
         "mar_noalloc_scratch_bytes": ([], SZ),
@@ -245,6 +248,50 @@ def mar_refresh_topk(score, exclude_idx, K: int, out_idx=None, active_out=None, 
     _check("mar_refresh_topk", rc)
     return out_idx
 
+
+
+def mar_refresh_topk_pairs(score, exclude_idx, K: int, out_idx=None, active_out=None, status=None, stream=None):
+    """Shared refresh set of guidance pairs: rows b and b + B/2 of score [B, N] take the top-K of
+    their fp32 summed scores. Returns out_idx [B, K] (both rows of a pair equal)."""
+    B2, N = score.shape
+    if B2 % 2:
+        raise ValueError("score needs an even number of rows (conditional, then unconditional)")
+    E = 0 if exclude_idx is None else int(exclude_idx.shape[1])
+    if out_idx is None:
+        out_idx = torch.empty(B2, K, dtype=torch.int32, device=score.device)
+    rc = load().mar_refresh_topk_pairs(B2 // 2, N, _ptr(score), _ptr(exclude_idx), E, int(K), _ptr(out_idx),
+                                       _ptr(active_out), _ptr(status), _stream(stream))
+    _check("mar_refresh_topk_pairs", rc)
+    return out_idx
+
+
+def mar_token_cosine(X, Y, out=None, stream=None):
+    """Per-token cosine similarity [B, N] of two [B, H, N, d] tensors (a token's values over all
+    heads); a [B, N, D] hidden state is passed as [B, 1, N, D]."""
+    lib = load()
+    if X.shape != Y.shape or X.dtype != Y.dtype:
+        raise ValueError("X and Y need the same shape and dtype")
+    s = _shape(X)
+    if out is None:
+        out = torch.empty(X.shape[0], X.shape[2], dtype=torch.float32, device=X.device)
+    rc = lib.mar_token_cosine(ctypes.byref(s), _ptr(X), _ptr(Y), _ptr(out), _stream(stream))
+    _check("mar_token_cosine", rc)
+    return out
+
+
+def mar_select_recompute(cos, tau: float, force_idx=None, out_idx=None, out_count=None, status=None, stream=None):
+    """Token-cache recompute set: (idx [B, N] ascending then -1, count [B]) of the positions with
+    not (cos > tau), or in force_idx [B, F]."""
+    B, N = cos.shape
+    F = 0 if force_idx is None else int(force_idx.shape[1])
+    if out_idx is None:
+        out_idx = torch.empty(B, N, dtype=torch.int32, device=cos.device)
+    if out_count is None:
+        out_count = torch.empty(B, dtype=torch.int32, device=cos.device)
+    rc = load().mar_select_recompute(B, N, _ptr(cos), float(tau), _ptr(force_idx), F, _ptr(out_idx),
+                                     _ptr(out_count), _ptr(status), _stream(stream))
+    _check("mar_select_recompute", rc)
+    return out_idx, out_count
 
 def mar_cfg_residual(mode: int, cond, uncond, residual, w: float | None = None, guided=None, stream=None):
     """LazyMAR condition cache: APPLY writes uncond, UPDATE writes residual."""

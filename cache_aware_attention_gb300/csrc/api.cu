@@ -239,6 +239,50 @@ int mar_refresh_topk(int32_t B, int32_t N, const float *score, const int32_t *ex
     return e == cudaSuccess ? MAR_OK : cuda_fail(e);
 }
 
+int mar_refresh_topk_pairs(int32_t B_pairs, int32_t N, const float *score, const int32_t *exclude_idx, int32_t E,
+                           int32_t K, int32_t *out_idx, int32_t *active_out, uint32_t *d_status,
+                           mar_stream_t stream) {
+    if (B_pairs < 0 || N < 0 || E < 0 || K < 0) return MAR_ERR_ARG;
+    if (N > 4096) return MAR_ERR_SHAPE;
+    if (E > N || K > N - E) return MAR_ERR_ARG;
+    if (B_pairs == 0 || N == 0) return MAR_OK;
+    if (!score || (E > 0 && !exclude_idx)) return MAR_ERR_ARG;
+    if (!out_idx && !active_out) return K == 0 ? MAR_OK : MAR_ERR_ARG;
+    mar::TopkParams p{};
+    p.score = score; p.exclude = exclude_idx; p.out = out_idx; p.active = active_out;
+    p.status = d_status; p.B = B_pairs; p.N = N; p.E = E; p.K = K; p.pairs = 1;
+    cudaError_t e = mar::launch_topk(p, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MAR_OK : cuda_fail(e);
+}
+
+int mar_token_cosine(const mar_shape *s, const void *X, const void *Y, float *cos_out, mar_stream_t stream) {
+    if (!s) return MAR_ERR_ARG;
+    if (s->B < 0 || s->H < 0 || s->N < 0 || s->d < 0) return MAR_ERR_ARG;
+    if (s->dtype != MAR_BF16 && s->dtype != MAR_F32) return MAR_ERR_DTYPE;
+    const int elem = s->dtype == MAR_BF16 ? 2 : 4;
+    if (s->d == 0 || (s->d * elem) % 16 != 0 || s->d > 16384) return MAR_ERR_SHAPE;
+    if (s->B == 0 || s->H == 0 || s->N == 0) return MAR_OK;
+    if (!X || !Y || !cos_out) return MAR_ERR_ARG;
+    if (!aligned16(X) || !aligned16(Y) || !aligned4(cos_out)) return MAR_ERR_ALIGN;
+    cudaError_t e = mar::launch_token_cosine(X, Y, cos_out, s->B, s->H, s->N, s->d, s->dtype == MAR_BF16,
+                                             reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MAR_OK : cuda_fail(e);
+}
+
+int mar_select_recompute(int32_t B, int32_t N, const float *cos, float tau, const int32_t *force_idx, int32_t F,
+                         int32_t *out_idx, int32_t *out_count, uint32_t *d_status, mar_stream_t stream) {
+    if (B < 0 || N < 0 || F < 0) return MAR_ERR_ARG;
+    if (N > 16384) return MAR_ERR_SHAPE;
+    if (B == 0 || N == 0) return MAR_OK;
+    if (!cos || !out_idx || !out_count || (F > 0 && !force_idx)) return MAR_ERR_ARG;
+    if (!aligned4(cos) || !aligned4(out_idx) || !aligned4(out_count)) return MAR_ERR_ALIGN;
+    mar::SelectParams p{};
+    p.cos = cos; p.force = F > 0 ? force_idx : nullptr; p.out = out_idx; p.count = out_count;
+    p.status = d_status; p.B = B; p.N = N; p.F = F; p.tau = tau;
+    cudaError_t e = mar::launch_select_recompute(p, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MAR_OK : cuda_fail(e);
+}
+
 int mar_cfg_residual(int32_t mode, int64_t n, const float *cond, float *uncond, float *residual,
                      float w, float *guided, mar_stream_t stream) {
     if (mode != MAR_CFG_APPLY && mode != MAR_CFG_UPDATE) return MAR_ERR_ARG;

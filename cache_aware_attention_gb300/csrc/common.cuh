@@ -104,6 +104,26 @@ MAR_DEVINL float max3f(float a, float b, float c) {
     return r;
 }
 
+// ---------------------------------------------------------------- double-float sums
+// (hi, lo) += x with the error-free two-sum, so that a sum of fp32 terms keeps about 48
+// bits (fp64-grade for these sums) without the fp64 pipe, which is slow on this part.
+// The result is a pure function of the operand sequence (deterministic).
+MAR_DEVINL void df_add(float &hi, float &lo, float x) {
+    const float s = hi + x;
+    const float bb = s - hi;
+    const float err = (hi - (s - bb)) + (x - bb);
+    hi = s;
+    lo += err;
+}
+// (hi, lo) += (hi2, lo2); symmetric in its operands (both sides of a butterfly agree)
+MAR_DEVINL void df_merge(float &hi, float &lo, float hi2, float lo2) {
+    const float s = hi + hi2;
+    const float bb = s - hi;
+    const float err = (hi - (s - bb)) + (hi2 - bb);
+    hi = s;
+    lo = (lo + lo2) + err;
+}
+
 // ---------------------------------------------------------------- active/cached partition
 // Builds, in shared memory, the ascending list of positions of one batch row that are
 // NOT in idx[0..A) (the cached set), using a bitmap of N bits. All threads of the

@@ -189,25 +189,6 @@ size_t cluster_smem_bytes(int N, int D, int elem) {
     return kbuf + sizeof(float) * ((size_t)2 * N + (size_t)kQReg * N);
 }
 
-// Double-float accumulation: (hi, lo) += x with the error-free two-sum, so that a sum of
-// fp32 terms keeps about 48 bits (fp64-grade for these sums) without the fp64 pipe, which
-// is slow on this part. The result is a pure function of the operand sequence.
-MAR_DEVINL void df_add(float &hi, float &lo, float x) {
-    const float s = hi + x;
-    const float bb = s - hi;
-    const float err = (hi - (s - bb)) + (x - bb);
-    hi = s;
-    lo += err;
-}
-// (hi, lo) += (hi2, lo2); symmetric in its operands (both sides of a butterfly agree)
-MAR_DEVINL void df_merge(float &hi, float &lo, float hi2, float lo2) {
-    const float s = hi + hi2;
-    const float bb = s - hi;
-    const float err = (hi - (s - bb)) + (hi2 - bb);
-    hi = s;
-    lo = (lo + lo2) + err;
-}
-
 template <typename T>
 MAR_DEVINL void load_chunk(const T *src, float (&v)[16 / sizeof(T)]) {
     const uint4 raw = *reinterpret_cast<const uint4 *>(src);

@@ -22,15 +22,33 @@ size_t score_smem_bytes(int N, int d);
 cudaError_t launch_score(const ScoreParams &p, cudaStream_t s);
 
 struct TopkParams {
-    const float *score;     // [B, N]
-    const int32_t *exclude; // [B, E] or nullptr
-    int32_t *out;           // [B, K] or nullptr
-    int32_t *active;        // [B, E + K] or nullptr
+    const float *score;     // [B, N] (pairs: [2B, N])
+    const int32_t *exclude; // [B, E] or nullptr (pairs: [2B, E])
+    int32_t *out;           // [B, K] or nullptr (pairs: [2B, K])
+    int32_t *active;        // [B, E + K] or nullptr (pairs: [2B, E + K])
     uint32_t *status;
-    int B, N, E, K;
+    int B, N, E, K;         // pairs: B = number of pairs
+    int pairs;              // rows b and b + B share one set, selected on the fp32 sum of their scores
 };
 
 cudaError_t launch_topk(const TopkParams &p, cudaStream_t s);
+
+// Token-cache recompute set: per row the positions with not (cos > tau), or forced,
+// ascending, then -1; count per row.
+struct SelectParams {
+    const float *cos;       // [B, N]
+    const int32_t *force;   // [B, F] or nullptr
+    int32_t *out;           // [B, N]
+    int32_t *count;         // [B]
+    uint32_t *status;
+    int B, N, F;
+    float tau;
+};
+cudaError_t launch_select_recompute(const SelectParams &p, cudaStream_t s);
+
+// Per-token cosine similarity of two [B, H, N, d] tensors over each token's H*d values.
+cudaError_t launch_token_cosine(const void *X, const void *Y, float *out, int B, int H, int N, int d, int is_bf16,
+                                cudaStream_t s);
 
 struct RowCopyParams {
     const void *src[3];

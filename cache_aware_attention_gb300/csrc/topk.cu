@@ -61,20 +61,36 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkParams p) {
 
     const int tid = threadIdx.x, b = blockIdx.x;
     const int N = p.N;
+    // pairs: rows b (conditional) and b + B (unconditional) share the selection, made on
+    // the fp32 sum of their scores with row b's exclusions
+    const int b2 = b + p.B;
     for (int j = tid; j < N; j += kThreads) {
-        keys[j] = order_key(p.score[(int64_t)b * N + j]);
+        const float sc = p.pairs ? __fadd_rn(p.score[(int64_t)b * N + j], p.score[(int64_t)b2 * N + j])
+                                 : p.score[(int64_t)b * N + j];
+        keys[j] = order_key(sc);
         cand[j] = 1;
     }
     __syncthreads();
     for (int e = tid; e < p.E; e += kThreads) {
         int pos = p.exclude[(int64_t)b * p.E + e];
-        if (p.active) p.active[(int64_t)b * (p.E + p.K) + e] = pos;  // copied as given
+        if (p.active) {
+            p.active[(int64_t)b * (p.E + p.K) + e] = pos;  // copied as given
+            if (p.pairs) p.active[(int64_t)b2 * (p.E + p.K) + e] = p.exclude[(int64_t)b2 * p.E + e];
+        }
         if (pos < 0 || pos >= N) {
             report(p.status, MAR_STATUS_INDEX_RANGE);
             continue;
         }
         cand[pos] = 0;
     }
+    auto emit = [&](int slot, int j) {
+        if (p.out) p.out[(int64_t)b * p.K + slot] = j;
+        if (p.active) p.active[(int64_t)b * (p.E + p.K) + p.E + slot] = j;
+        if (p.pairs) {
+            if (p.out) p.out[(int64_t)b2 * p.K + slot] = j;
+            if (p.active) p.active[(int64_t)b2 * (p.E + p.K) + p.E + slot] = j;
+        }
+    };
     if (p.K == 0) return;
     if (N <= kRankN) {
         // rank = number of candidates before j in (key desc, position asc) order; one
@@ -96,10 +112,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkParams p) {
             int tot;
             const int slot = base + block_excl_scan(sel ? 1 : 0, warp_sums, &tot);
             base += tot;
-            if (sel && slot < p.K) {
-                if (p.out) p.out[(int64_t)b * p.K + slot] = j;
-                if (p.active) p.active[(int64_t)b * (p.E + p.K) + p.E + slot] = j;
-            }
+            if (sel && slot < p.K) emit(slot, j);
         }
         return;
     }
@@ -145,11 +158,44 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkParams p) {
         const bool sel = c && (keys[j] > T || (eq && eq_rank < take));
         const int slot = out_base + block_excl_scan(sel ? 1 : 0, warp_sums, &tot);
         out_base += tot;
-        if (sel && slot < p.K) {
-            if (p.out) p.out[(int64_t)b * p.K + slot] = j;
-            if (p.active) p.active[(int64_t)b * (p.E + p.K) + p.E + slot] = j;
-        }
+        if (sel && slot < p.K) emit(slot, j);
     }
+}
+
+constexpr int kSelectMaxN = 16384;
+
+// Token-cache recompute set (LazyMAR notes, Token Cache): one CTA per row; position j is
+// recomputed when it is forced or not (cos > tau) (a NaN similarity is recomputed). The
+// positions are written in ascending order by a block-wide prefix sum, the remaining
+// slots get -1.
+__global__ void __launch_bounds__(kThreads) select_recompute_kernel(SelectParams p) {
+    __shared__ uint32_t forced[kSelectMaxN / 32];
+    __shared__ int warp_sums[kThreads / 32];
+    const int tid = threadIdx.x, b = blockIdx.x, N = p.N;
+    const int words = (N + 31) >> 5;
+    for (int w = tid; w < words; w += kThreads) forced[w] = 0u;
+    __syncthreads();
+    for (int f = tid; f < p.F; f += kThreads) {
+        const int pos = p.force[(int64_t)b * p.F + f];
+        if (pos < 0 || pos >= N) {
+            report(p.status, MAR_STATUS_INDEX_RANGE);
+            continue;
+        }
+        atomicOr(&forced[pos >> 5], 1u << (pos & 31));
+    }
+    __syncthreads();
+    int base = 0;
+    for (int j0 = 0; j0 < N; j0 += kThreads) {
+        const int j = j0 + tid;
+        bool sel = false;
+        if (j < N) sel = ((forced[j >> 5] >> (j & 31)) & 1u) || !(p.cos[(int64_t)b * N + j] > p.tau);
+        int tot;
+        const int slot = base + block_excl_scan(sel ? 1 : 0, warp_sums, &tot);
+        base += tot;
+        if (sel) p.out[(int64_t)b * N + slot] = j;
+    }
+    for (int j = base + tid; j < N; j += kThreads) p.out[(int64_t)b * N + j] = -1;
+    if (tid == 0) p.count[b] = base;
 }
 
 }  // namespace
@@ -157,6 +203,17 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkParams p) {
 cudaError_t launch_topk(const TopkParams &p, cudaStream_t s) {
     if (p.N > kMaxN) return cudaErrorInvalidValue;
     topk_kernel<<<p.B, kThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace mar
+
+namespace mar {
+
+cudaError_t launch_select_recompute(const SelectParams &p, cudaStream_t s) {
+    if (p.N > kSelectMaxN) return cudaErrorInvalidValue;
+    if (p.B == 0 || p.N == 0) return cudaSuccess;
+    select_recompute_kernel<<<p.B, kThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

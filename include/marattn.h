@@ -240,6 +240,59 @@ int mar_refresh_topk(int32_t B, int32_t N, const float *score, const int32_t *ex
                      uint32_t *d_status, mar_stream_t stream);
 
 /*
+ * mar_refresh_topk_pairs -- one refresh set per classifier-free-guidance pair.
+ *
+ * [M] Key Design 1 selects the refreshing tokens per batch row; the pages do not say
+ * whether, with guidance, the conditional row b and the unconditional row
+ * b + B_pairs select separately or share one set. This call is the shared reading
+ * (mar_refresh_topk is the separate one): the pair's candidates are
+ * ranked on the fp32 sum of the two rows' scores (one IEEE single addition per
+ * position), with row b's exclusions, ties to the lower position, output ascending.
+ * Both rows receive the same set; each row's active_out starts with its own exclusions.
+ *  score        [2*B_pairs, N] fp32 (rows [0, B_pairs) conditional, then unconditional).
+ *  exclude_idx  [2*B_pairs, E] int32; out_idx [2*B_pairs, K] and/or active_out
+ *               [2*B_pairs, E + K]. Limits and errors as for mar_refresh_topk.
+ */
+int mar_refresh_topk_pairs(int32_t B_pairs, int32_t N, const float *score, const int32_t *exclude_idx,
+                           int32_t E, int32_t K, int32_t *out_idx, int32_t *active_out,
+                           uint32_t *d_status, mar_stream_t stream);
+
+/*
+ * mar_token_cosine -- per-token cosine similarity of two feature tensors.
+ *
+ * [L] Token Cache: deeper layers reuse a token's cached value when its current
+ * feature is close, in cosine similarity, to the cached one. [M] Figure 1 and
+ * Figures 10-11: the cosine of the key (value) projections between decoding steps,
+ * which shows the drift that cached attention tolerates. A token's feature is its
+ * values over all heads:
+ *   cos[b,n] = <X[b,:,n,:], Y[b,:,n,:]> / (|X[b,:,n,:]| |Y[b,:,n,:]|)
+ * both zero -> 1, one zero -> 0. Sums are carried to fp64-grade accuracy in a fixed
+ * order (deterministic); the result is fp32.
+ *  X, Y     [B,H,N,d] (dtype); any d with d * element size a multiple of 16 bytes,
+ *           d <= 16384 (H = 1 with d = the model width for a [B,N,D] hidden state).
+ *  cos_out  [B,N] fp32.
+ */
+int mar_token_cosine(const mar_shape *shape, const void *X, const void *Y, float *cos_out,
+                     mar_stream_t stream);
+
+/*
+ * mar_select_recompute -- the token cache's recompute set.
+ *
+ * [L] Token Cache: tokens with a high similarity to the cached feature reuse the
+ * cached value; the others are recomputed. Here position n of row b is recomputed
+ * when it is in force_idx[b] or when not (cos[b,n] > tau) (a NaN similarity is
+ * recomputed); the decision is taken on the given fp32 values.
+ *  cos        [B,N] fp32 (e.g. from mar_token_cosine); N <= 16384.
+ *  force_idx  [B,F] int32 or NULL when F == 0 (e.g. the tokens decoded this step);
+ *             out-of-range entries set MAR_STATUS_INDEX_RANGE and are ignored.
+ *  out_idx    [B,N] int32: the recomputed positions in ascending order, then -1.
+ *  out_count  [B] int32: how many.
+ */
+int mar_select_recompute(int32_t B, int32_t N, const float *cos, float tau, const int32_t *force_idx,
+                         int32_t F, int32_t *out_idx, int32_t *out_count, uint32_t *d_status,
+                         mar_stream_t stream);
+
+/*
  * mar_cfg_residual -- LazyMAR condition cache on fp32 outputs of n elements.
  *
  * [L] Condition Cache: a cached step runs only the conditional branch and

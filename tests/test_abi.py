@@ -122,3 +122,22 @@ def test_attn_full_refresh_validation(lib):
     assert call(_shape(), vc=FAKE + 1024) == -1     # V cache aliases K cache
     assert call(_shape(), vc=FAKE + 1288) == -4     # misaligned cache
     assert call(_shape(B=0)) == 0                   # empty: no-op
+
+
+def test_next_rows_validation(lib):
+    sh = lambda **k: _shape(**k)
+    # token cosine: any d with whole 16-byte chunks
+    assert lib.mar_token_cosine(sh(d=12), FAKE, FAKE, FAKE, None) == -2          # 24 bytes per row
+    assert lib.mar_token_cosine(sh(dtype=7), FAKE, FAKE, FAKE, None) == -3
+    assert lib.mar_token_cosine(sh(), None, FAKE, FAKE, None) == -1
+    assert lib.mar_token_cosine(sh(), FAKE + 8, FAKE, FAKE, None) == -4
+    assert lib.mar_token_cosine(sh(B=0), None, None, None, None) == 0
+    # recompute set
+    assert lib.mar_select_recompute(2, 16385, FAKE, 0.5, None, 0, FAKE, FAKE, None, None) == -2
+    assert lib.mar_select_recompute(2, 10, FAKE, 0.5, None, 3, FAKE, FAKE, None, None) == -1   # F > 0, no force
+    assert lib.mar_select_recompute(-1, 10, FAKE, 0.5, None, 0, FAKE, FAKE, None, None) == -1
+    assert lib.mar_select_recompute(0, 10, None, 0.5, None, 0, None, None, None, None) == 0
+    # shared refresh set
+    assert lib.mar_refresh_topk_pairs(2, 4097, FAKE, FAKE, 1, 1, FAKE, None, None, None) == -2
+    assert lib.mar_refresh_topk_pairs(2, 10, FAKE, FAKE, 5, 6, FAKE, None, None, None) == -1   # K > N - E
+    assert lib.mar_refresh_topk_pairs(2, 10, FAKE, FAKE, 2, 3, None, None, None, None) == -1   # no output

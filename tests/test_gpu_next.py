@@ -1,0 +1,139 @@
+"""GPU parity of the next rows: token similarity (KV drift, LazyMAR token cache), the
+token cache's recompute set, and the shared refresh set of guidance pairs.
+
+Inputs come from the seeded generators in ``workloads``; expected values only from
+``oracle``. Where a float decides an index (a threshold, a ranking) the oracle takes the
+decision on the same fp32 values the GPU produced, and the fp32 values themselves are
+checked against the fp64 oracle separately.
+"""
+import numpy as np
+import pytest
+import torch
+
+import cache_aware_attention_gb300 as mar
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from cache_aware_attention_gb300 import _build
+    _build.build()
+    mar.load()
+    oracle.build()
+
+
+def _rand(shape, seed, dtype, std=1.0):
+    return workloads.normal(shape, seed, dtype, DEV, std=std)
+
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+# ------------------------------------------------------------------------------ token cosine
+@pytest.mark.parametrize("B,H,N,d,dtype,drift", [
+    (4, 12, 320, 64, torch.bfloat16, 0.05),    # MAR-B key projections, one step of drift
+    (3, 1, 50, 768, torch.bfloat16, 0.2),      # a [B, N, D] hidden state (LazyMAR token cache)
+    (2, 4, 77, 32, torch.float32, 0.5),
+    (2, 3, 65, 8, torch.bfloat16, 1.0),        # one 16-byte chunk per head row
+    (1, 16, 1088, 80, torch.bfloat16, 0.05),   # 512 px shape
+])
+def test_token_cosine(B, H, N, d, dtype, drift):
+    X = _rand((B, H, N, d), 700, torch.float32)
+    Y = (X + drift * _rand((B, H, N, d), 701, torch.float32)).to(dtype)
+    X = X.to(dtype)
+    if N > 10:                                   # some tokens: zero in one or both tensors
+        X[0, :, 3] = 0
+        Y[0, :, 3] = 0
+        X[-1, :, 7] = 0
+        Y[0, :, 9] = 0
+    got = mar.mar_token_cosine(X.contiguous(), Y.contiguous())
+    ref = oracle.token_cosine(X, Y)
+    err = np.abs(got.cpu().numpy().astype(np.float64) - ref)
+    assert err.max() <= 1e-6, f"max |cos - ref| = {err.max():.3g}"
+
+
+def test_token_cosine_is_deterministic():
+    X = _rand((2, 12, 320, 64), 702, torch.bfloat16)
+    Y = _rand((2, 12, 320, 64), 703, torch.bfloat16)
+    a = mar.mar_token_cosine(X, Y)
+    b = mar.mar_token_cosine(X, Y)
+    assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------------------ recompute set
+@pytest.mark.parametrize("B,N,F,tau", [(4, 320, 4, 0.99), (3, 1088, 0, 0.95), (2, 16384, 30, 0.5),
+                                        (5, 64, 64, 0.0), (2, 1, 0, 0.3)])
+def test_select_recompute_bit_exact(B, N, F, tau):
+    g = np.random.default_rng(N + F)
+    cos = (1.0 - g.random((B, N)) ** 3 * 0.2).astype(np.float32)   # mostly close to 1
+    cos[0, : min(N, 5)] = np.float32(tau)                         # equal to the threshold
+    if N > 8:
+        cos[-1, 6] = np.nan
+    force = np.stack([g.permutation(N)[:F] for _ in range(B)]).astype(np.int32) if F else None
+    c = torch.from_numpy(cos).to(DEV)
+    f = torch.from_numpy(force).to(DEV) if F else None
+    st = _status()
+    idx, cnt = mar.mar_select_recompute(c, tau, f, status=st)
+    assert mar.mar_status_read(st) == 0
+    ref_idx, ref_cnt = oracle.select_recompute(cos, tau, force)
+    np.testing.assert_array_equal(cnt.cpu().numpy(), ref_cnt)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+
+
+def test_select_recompute_on_gpu_similarities():
+    # the token-cache flow: similarity of this step's features to the cached ones, then the
+    # recompute set with the tokens decoded this step forced in
+    B, N, D = 4, 320, 768
+    cached = _rand((B, 1, N, D), 710, torch.float32)
+    moved = torch.zeros(B, N, dtype=torch.bool)
+    moved[:, 64:80] = True                                        # the just-decoded tokens move
+    cur = cached + 0.02 * _rand((B, 1, N, D), 711, torch.float32)
+    cur[:, :, 64:80] += 1.0 * _rand((B, 1, 16, D), 712, torch.float32)
+    cached, cur = cached.to(torch.bfloat16), cur.to(torch.bfloat16)
+    cos = mar.mar_token_cosine(cur, cached)
+    force = workloads.distinct_positions(B, 4, 100, N, 713).to(DEV)
+    idx, cnt = mar.mar_select_recompute(cos, 0.99, force)
+    ref_idx, ref_cnt = oracle.select_recompute(cos.cpu().numpy(), 0.99, force.cpu().numpy())
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    np.testing.assert_array_equal(cnt.cpu().numpy(), ref_cnt)
+    sel = [set(r[:c].tolist()) for r, c in zip(idx.cpu().numpy(), cnt.cpu().numpy())]
+    for b in range(B):
+        assert set(range(64, 80)) <= sel[b]                       # every moved token recomputed
+        assert set(force[b].tolist()) <= sel[b]
+
+
+def test_select_recompute_reports_bad_force():
+    cos = torch.ones(2, 10, device=DEV)
+    st = _status()
+    idx, cnt = mar.mar_select_recompute(cos, 0.5, torch.tensor([[3], [12]], dtype=torch.int32, device=DEV), status=st)
+    assert mar.mar_status_read(st) & mar.MAR_STATUS_INDEX_RANGE
+    assert cnt.cpu().tolist() == [1, 0]
+
+
+# ------------------------------------------------------------------------------ shared refresh set
+@pytest.mark.parametrize("Bp,N,E,K,levels", [(32, 320, 8, 32, 0), (32, 320, 8, 32, 4), (4, 1088, 50, 64, 0),
+                                              (3, 4096, 10, 500, 0), (2, 20, 3, 0, 0)])
+def test_refresh_topk_pairs_bit_exact(Bp, N, E, K, levels):
+    g = np.random.default_rng(N + E + K)
+    sc = g.random((2 * Bp, N)).astype(np.float32)
+    if levels:
+        sc = (np.floor(sc * levels) / levels).astype(np.float32)  # many exact ties
+    ex = np.stack([g.permutation(N)[:E] for _ in range(Bp)]).astype(np.int32).reshape(Bp, E)
+    ex = np.concatenate([ex, ex], 0)
+    score = torch.from_numpy(sc).to(DEV)
+    exd = torch.from_numpy(ex).to(DEV) if E else None
+    active = torch.empty(2 * Bp, E + K, dtype=torch.int32, device=DEV)
+    R = mar.mar_refresh_topk_pairs(score, exd, K, active_out=active)
+    if K == 0:
+        return
+    ref = oracle.topk_pairs(sc, ex, K)
+    np.testing.assert_array_equal(R.cpu().numpy(), ref)
+    np.testing.assert_array_equal(active.cpu().numpy(), np.concatenate([ex, ref], 1))
