@@ -30,6 +30,16 @@ int check_shape(const mar_shape *s) {
     return MAR_OK;
 }
 
+// Row copies take any row of whole 16-byte vectors (up to 16384 elements), e.g. hidden
+// states [B, 1, N, D] of a token cache.
+int check_rows_shape(const mar_shape *s) {
+    if (!s) return MAR_ERR_ARG;
+    if (s->dtype != MAR_F32 && s->dtype != MAR_BF16) return MAR_ERR_DTYPE;
+    if (s->B < 0 || s->H < 0 || s->N < 0 || s->d < 0) return MAR_ERR_ARG;
+    if (s->d == 0 || s->d > 16384 || (s->d * (int)elem_size(s->dtype)) % 16 != 0) return MAR_ERR_SHAPE;
+    return MAR_OK;
+}
+
 constexpr size_t kWsAlign = 256;
 size_t round_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
 
@@ -183,7 +193,7 @@ int mar_attn_cache_aware(const mar_shape *s, int32_t A, const void *Q_A, const v
 
 static int rows_common(const mar_shape *s, int32_t A, int n, const void *const *src, void *const *dst,
                        const int32_t *idx, int scatter, uint32_t *d_status, mar_stream_t stream) {
-    int rc = check_shape(s);
+    int rc = check_rows_shape(s);
     if (rc != MAR_OK) return rc;
     if (A < 0 || A > s->N || n < 1 || n > 3) return MAR_ERR_ARG;
     if (!idx && A != s->N) return MAR_ERR_ARG;

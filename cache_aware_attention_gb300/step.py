@@ -18,7 +18,7 @@ from __future__ import annotations
 import torch
 
 from . import (mar_attn_cache_aware, mar_attn_full, mar_attn_full_refresh, mar_attn_full_workspace_bytes,
-               mar_kv_gather, mar_refresh_topk)
+               mar_kv_gather, mar_refresh_topk, mar_refresh_topk_pairs)
 
 REFRESH_PERIOD = 3
 
@@ -33,15 +33,25 @@ class DecodeStep:
 
     Shapes: fresh Q/K/V of each layer and the layer-3 cache are [B', H, N, d];
     ``exclude`` is the host schedule's [B', G+J] int32 device tensor (generating then
-    just-decoded positions). ``K`` refresh tokens per row; ``a_max`` bounds G+J+K."""
+    just-decoded positions). ``K`` refresh tokens per row; ``a_max`` bounds G+J+K.
+
+    ``budget``: the fixed-budget form of the refresh count (MARché Key Design 1 and the
+    latency/FID trade-off of Figure 6 speak of a fixed number of active tokens per step):
+    K = budget - (G + J) at each step instead of a fixed K. ``shared_pairs``: rows b and
+    b + B'/2 (conditional and unconditional halves of a guidance batch) share one refresh
+    set, ranked on the sum of their scores."""
 
     def __init__(self, B: int, H: int, N: int, d: int, K: int, a_max: int, dtype=torch.bfloat16,
-                 device="cuda", max_gen: int | None = None):
+                 device="cuda", max_gen: int | None = None, budget: int | None = None,
+                 shared_pairs: bool = False):
+        if shared_pairs and B % 2:
+            raise ValueError("shared_pairs needs an even number of rows")
         self.B, self.H, self.N, self.d, self.K, self.a_max = B, H, N, d, K, a_max
+        self.budget, self.shared_pairs = budget, shared_pairs
         self.device = torch.device(device)
         dev, f32, i32 = self.device, torch.float32, torch.int32
         self.score = torch.empty(B, N, dtype=f32, device=dev)
-        self.R = torch.empty(B, K, dtype=i32, device=dev)
+        self._R = torch.empty(B * max(K, budget or 0, 1), dtype=i32, device=dev)
         self._active = torch.empty(B * a_max, dtype=i32, device=dev)
         self._qkv = [torch.empty(B * H * a_max * d, dtype=dtype, device=dev) for _ in range(3)]
         self._oa = torch.empty(B * H * a_max * d, dtype=dtype, device=dev)
@@ -51,6 +61,19 @@ class DecodeStep:
         ws = mar_attn_full_workspace_bytes(probe, max_gen or N, True)
         self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def refresh_count(self, n_exclude: int) -> int:
+        """K of a cached step: fixed, or budget - (G + J) (at least 0, at most the candidates)."""
+        if self.budget is None:
+            return self.K
+        return max(0, min(self.budget - n_exclude, self.N - n_exclude))
+
+    @property
+    def R(self) -> torch.Tensor:
+        return self._R[: self.B * self.K].view(self.B, self.K)
+
+    def refresh_set(self, K: int) -> torch.Tensor:
+        return self._R[: self.B * K].view(self.B, K)
 
     def active(self, A: int) -> torch.Tensor:
         return self._active[: self.B * A].view(self.B, A)
@@ -73,12 +96,16 @@ class DecodeStep:
             # layer 3: full attention and the whole-cache overwrite in one call
             mar_attn_full_refresh(Q3, K3, V3, Kc, Vc, self.O3, status=self.status, stream=stream)
             return ("full", self.O3)
-        A = exclude.shape[1] + self.K
+        K = self.refresh_count(exclude.shape[1])
+        A = exclude.shape[1] + K
+        if A > self.a_max:
+            raise ValueError(f"active set of {A} exceeds a_max = {self.a_max}")
         act = self.active(A)
         mar_attn_full(Q2, K2, V2, self.O2, gen_idx=gen, score_out=self.score, workspace=self.workspace,
                       status=self.status, stream=stream)
-        mar_refresh_topk(self.score, exclude, self.K, out_idx=self.R, active_out=act,
-                         status=self.status, stream=stream)
+        select = mar_refresh_topk_pairs if self.shared_pairs else mar_refresh_topk
+        select(self.score, exclude, K, out_idx=self.refresh_set(K), active_out=act, status=self.status,
+               stream=stream)
         return self.cached_layer(A, layer3, cache, stream=stream)
 
     def cached_layer(self, A: int, layer3, cache, stream=None):

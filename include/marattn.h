@@ -77,7 +77,7 @@ typedef struct mar_shape {
     int32_t B;     /* batch rows (after CFG doubling) */
     int32_t H;     /* heads */
     int32_t N;     /* tokens per row (buffer + image tokens) */
-    int32_t d;     /* head dim: 32, 64, 80 or 128 */
+    int32_t d;     /* head dim: 32, 64, 80 or 128 (attention); see the row copies */
     int32_t dtype; /* enum mar_dtype */
 } mar_shape;
 
@@ -205,7 +205,10 @@ int mar_attn_cache_aware(const mar_shape *shape, int32_t A, const void *Q_A,
  *   K_cache[b,h,active_idx[b,a],:] = K_A[b,h,a,:]   (V likewise; bit copies)
  * active_idx == NULL with A == N overwrites every row in order (full refresh).
  * Either the K pair or the V pair may be NULL to skip that tensor. Repeated
- * positions leave it unspecified which row lands.
+ * positions leave it unspecified which row lands. Row copies (this call and
+ * mar_kv_gather) take any d whose row is whole 16-byte vectors, d <= 16384 (e.g. a
+ * [B, 1, N, D] hidden state of a token cache); out-of-range positions set
+ * MAR_STATUS_INDEX_RANGE and are skipped.
  */
 int mar_kv_scatter(const mar_shape *shape, int32_t A, const void *K_A, const void *V_A,
                    const int32_t *active_idx, void *K_cache, void *V_cache,

@@ -137,3 +137,58 @@ def test_refresh_topk_pairs_bit_exact(Bp, N, E, K, levels):
     ref = oracle.topk_pairs(sc, ex, K)
     np.testing.assert_array_equal(R.cpu().numpy(), ref)
     np.testing.assert_array_equal(active.cpu().numpy(), np.concatenate([ex, ref], 1))
+
+
+# ------------------------------------------------------------------------------ step policies
+def test_decode_step_budget_and_shared_pairs():
+    from cache_aware_attention_gb300.step import DecodeStep
+    cfg = workloads.CONFIGS["mar_b"]
+    Bp, H, N, d = 8, cfg.H, cfg.N, cfg.d                 # 4 guidance pairs
+    ss = workloads.single_step(cfg.scaled(B=Bp // 2), device=DEV, seed=720)
+    G, J, budget = 4, 4, 64
+    pos = workloads.distinct_positions(Bp // 2, G + J, cfg.n_buf, N, 721)
+    pos = torch.cat([pos, pos], 0).to(DEV)
+    gen, excl = pos[:, :G].contiguous(), pos.contiguous()
+    step = DecodeStep(Bp, H, N, d, 0, budget, device=DEV, max_gen=G, budget=budget, shared_pairs=True)
+    Kc0, Vc0 = ss.Kc.clone(), ss.Vc.clone()
+    kind, oa, act = step.run(1, (ss.Q2, ss.K2, ss.V2), (ss.Q3, ss.K3, ss.V3), (ss.Kc, ss.Vc), gen, excl)
+    torch.cuda.synchronize()
+    assert kind == "cached" and act.shape == (Bp, budget)
+    R = act[:, G + J:].cpu().numpy()
+    np.testing.assert_array_equal(R[: Bp // 2], R[Bp // 2:])          # pairs share the set
+    np.testing.assert_array_equal(R, oracle.topk_pairs(step.score.cpu().numpy(), excl.cpu().numpy(),
+                                                       budget - G - J))
+    # the cache-aware output of a sampled row against the oracle, on the pre-step cache
+    b = 5
+    a = act[b:b + 1].cpu()
+    qa, ka, va = (torch.stack([x[b][:, a[0].long()].cpu()]) for x in (ss.Q3, ss.K3, ss.V3))
+    O_ref, _ = oracle.cache_aware(qa, ka, va, Kc0[b:b + 1].cpu(), Vc0[b:b + 1].cpu(), a)
+    got = oa[b:b + 1].float().cpu().numpy()
+    assert np.abs(got - O_ref).max() < 2e-2
+
+
+def test_kv_drift_and_stale_attention_error_over_steps():
+    # MARche notes, Figure 1 / Figures 10-11 and Key Design 3: the keys drift from step to
+    # step; between refreshes the cache goes stale and the cached path's error grows; a
+    # refresh brings it back to zero.
+    from cache_aware_attention_gb300.policy import kv_drift, stale_attention_error
+    B, H, N, d, A = 4, 12, 320, 64, 40
+    K = _rand((B, H, N, d), 730, torch.float32)
+    V = _rand((B, H, N, d), 731, torch.float32)
+    Kc, Vc = K.to(torch.bfloat16), V.to(torch.bfloat16)
+    errs, coss = [], []
+    for t in range(1, 7):
+        K = K + 0.05 * _rand((B, H, N, d), 740 + t, torch.float32)
+        V = V + 0.05 * _rand((B, H, N, d), 760 + t, torch.float32)
+        Kf, Vf = K.to(torch.bfloat16), V.to(torch.bfloat16)
+        if t % 3 == 0:
+            Kc, Vc = Kf.clone(), Vf.clone()              # full refresh
+        ck, cv = kv_drift(Kc, Kf, Vc, Vf)
+        coss.append(float(ck.mean()))
+        idx = workloads.distinct_positions(B, A, 0, N, 780 + t).to(DEV)
+        QA = _rand((B, H, A, d), 790 + t, torch.bfloat16)
+        KA, VA = mar.mar_kv_gather([Kf, Vf], idx)
+        errs.append(stale_attention_error(QA, KA, VA, (Kc, Vc), (Kf, Vf), idx))
+    assert errs[2] < 1e-6 and errs[5] < 1e-6             # refreshed at t = 3 and 6: current cache
+    assert 0 < errs[0] < errs[1] and 0 < errs[3] < errs[4]
+    assert coss[2] == pytest.approx(1.0, abs=1e-6) and coss[0] > coss[1] and coss[3] > coss[4]
