@@ -297,6 +297,10 @@ def breakdown(args, cfg, sets, step, mar, W, K, is_full_refresh, reps: int = 24)
     A = cfg.A
     act = step.active(A)
     qa, ka, va, oa = (step.dense(i, A) for i in range(4))
+    dev = step.score.device
+    cos_buf = torch.empty(cfg.Bp, cfg.N, dtype=torch.float32, device=dev)
+    sel_idx = torch.empty(cfg.Bp, cfg.N, dtype=torch.int32, device=dev)
+    sel_cnt = torch.empty(cfg.Bp, dtype=torch.int32, device=dev)
     calls = {
         "attn_full": lambda s: mar.mar_attn_full(s.layer2[0], s.layer2[1], s.layer2[2], step.O2),
         "attn_full+score": lambda s: mar.mar_attn_full(s.layer2[0], s.layer2[1], s.layer2[2], step.O2,
@@ -309,6 +313,13 @@ def breakdown(args, cfg, sets, step, mar, W, K, is_full_refresh, reps: int = 24)
         "attn_full_refresh": lambda s: mar.mar_attn_full_refresh(s.layer3[0], s.layer3[1], s.layer3[2], s.cache[0],
                                                                  s.cache[1], step.O3),
         "cfg": lambda s: mar.mar_cfg_residual(mar.MAR_CFG_APPLY, s.cond, s.uncond, s.residual),
+        # next rows, outside the step: KV-drift cosine of the layer-3 cache against the fresh
+        # keys, the token cache's recompute set on those similarities, the shared refresh set
+        "token_cosine": lambda s: mar.mar_token_cosine(s.cache[0], s.layer3[1], out=cos_buf),
+        "select_recompute": lambda s: mar.mar_select_recompute(cos_buf, 0.999, s.exclude, out_idx=sel_idx,
+                                                               out_count=sel_cnt),
+        "topk_pairs": lambda s: mar.mar_refresh_topk_pairs(step.score, s.exclude, cfg.K, out_idx=step.R,
+                                                           active_out=act),
     }
     algo = {"attn_full": bytes_full_attention(cfg),
             "attn_full+score": bytes_full_attention(cfg),
@@ -316,7 +327,10 @@ def breakdown(args, cfg, sets, step, mar, W, K, is_full_refresh, reps: int = 24)
             "gather": 2 * 3 * cfg.Bp * cfg.H * A * cfg.d * 2,
             "cache_aware": bytes_cache_aware(cfg, A) + 2 * cfg.Bp * cfg.H * A * cfg.d * 2,
             "attn_full_refresh": bytes_full_attention(cfg) + 2 * cfg.Bp * cfg.H * cfg.N * cfg.d * 2,
-            "cfg": 3 * cfg.B * cfg.n_img * cfg.latent * 4}
+            "cfg": 3 * cfg.B * cfg.n_img * cfg.latent * 4,
+            "token_cosine": 2 * cfg.Bp * cfg.H * cfg.N * cfg.d * 2 + cfg.Bp * cfg.N * 4,
+            "select_recompute": cfg.Bp * cfg.N * 4 * 2 + cfg.Bp * (cfg.G + cfg.J) * 4,
+            "topk_pairs": cfg.Bp * cfg.N * 4 + cfg.Bp * (cfg.G + cfg.J + cfg.K) * 4}
     side = torch.cuda.Stream()
     out = {}
     for name, fn in calls.items():
