@@ -281,7 +281,7 @@ def run_mine(args, ws, rank, local):
 
 
 def launches_per_step(t):
-    # refresh: attn(L2) + attn with cache refresh (L3) + cfg = 3; cached: attn + score + topk +
+    # refresh: attn(L2) + attn with cache refresh (L3) + cfg = 3; cached: attn + score + top-K +
     # gather + cache-aware + cfg = 6
     return 3 if t % REFRESH_PERIOD == 0 else 6
 
@@ -307,6 +307,9 @@ def breakdown(args, cfg, sets, step, mar, W, K, is_full_refresh, reps: int = 24)
                                                        gen_idx=s.gen, score_out=step.score,
                                                        workspace=step.workspace),
         "topk": lambda s: mar.mar_refresh_topk(step.score, s.exclude, cfg.K, out_idx=step.R, active_out=act),
+        "attn_full_select": lambda s: mar.mar_attn_full_select(s.layer2[0], s.layer2[1], s.layer2[2], s.gen, s.exclude,
+                                                               cfg.K, step.score, O=step.O2, out_idx=step.R,
+                                                               active_out=act, workspace=step.workspace),
         "gather": lambda s: mar.mar_kv_gather(list(s.layer3), act, dsts=[qa, ka, va]),
         "cache_aware": lambda s: mar.mar_attn_cache_aware(qa, ka, va, s.cache[0], s.cache[1], act, O_A=oa,
                                                           fuse_scatter=True),
@@ -324,6 +327,7 @@ def breakdown(args, cfg, sets, step, mar, W, K, is_full_refresh, reps: int = 24)
     algo = {"attn_full": bytes_full_attention(cfg),
             "attn_full+score": bytes_full_attention(cfg),
             "topk": cfg.Bp * cfg.N * 4 + cfg.Bp * (cfg.G + cfg.J + cfg.K) * 4,
+            "attn_full_select": bytes_full_attention(cfg),
             "gather": 2 * 3 * cfg.Bp * cfg.H * A * cfg.d * 2,
             "cache_aware": bytes_cache_aware(cfg, A) + 2 * cfg.Bp * cfg.H * A * cfg.d * 2,
             "attn_full_refresh": bytes_full_attention(cfg) + 2 * cfg.Bp * cfg.H * cfg.N * cfg.d * 2,

@@ -69,6 +69,7 @@ def load(path: str | None = None):
         "mar_attn_full_workspace_bytes": ([SP, I32, ctypes.c_int], SZ),
         "mar_attn_full": ([SP, P, P, P, P, F, P, I32, P, P, P, SZ, P, P], ctypes.c_int),
         "mar_attn_full_refresh": ([SP, P, P, P, P, P, P, F, P, P, P], ctypes.c_int),
+        "mar_attn_full_select": ([SP, P, P, P, P, F, P, I32, P, I32, I32, P, P, P, P, P, SZ, P, P], ctypes.c_int),
         "mar_attn_cache_aware_workspace_bytes": ([SP, I32], SZ),
         "mar_attn_cache_aware": ([SP, I32, P, P, P, P, P, P, P, F, P, I32, P, SZ, P, P], ctypes.c_int),
         "mar_kv_scatter": ([SP, I32, P, P, P, P, P, P, P], ctypes.c_int),
@@ -157,6 +158,30 @@ def mar_attn_full(Q, K, V, O=None, scale: float = 0.0, gen_idx=None, score_out=N
                            _ptr(gen_idx), G, _ptr(score_out), _ptr(lse_out), _ptr(workspace), wb,
                            _ptr(status), _stream(stream))
     _check("mar_attn_full", rc)
+    return O
+
+
+def mar_attn_full_select(Q, K, V, gen_idx, exclude_idx, Ksel: int, score_out, O=None, out_idx=None,
+                         active_out=None, scale: float = 0.0, lse_out=None, workspace=None, status=None,
+                         stream=None):
+    """Layer-2 call of a cached step: full attention, the score [B,N] and the refresh set
+    out_idx [B,Ksel] / active set active_out [B,E+Ksel] on it (mar_attn_full followed by
+    mar_refresh_topk, as one call). Returns O."""
+    lib = load()
+    s = _shape(Q)
+    if O is None:
+        O = torch.empty_like(Q)
+    G = int(gen_idx.shape[1])
+    E = 0 if exclude_idx is None else int(exclude_idx.shape[1])
+    need = lib.mar_attn_full_workspace_bytes(ctypes.byref(s), G, 1)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+    wb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.mar_attn_full_select(ctypes.byref(s), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), float(scale),
+                                  _ptr(gen_idx), G, _ptr(exclude_idx), E, int(Ksel), _ptr(score_out),
+                                  _ptr(out_idx), _ptr(active_out), _ptr(lse_out), _ptr(workspace), wb,
+                                  _ptr(status), _stream(stream))
+    _check("mar_attn_full_select", rc)
     return O
 
 

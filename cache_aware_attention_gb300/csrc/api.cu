@@ -82,9 +82,13 @@ size_t mar_attn_full_workspace_bytes(const mar_shape *s, int32_t G, int want_sco
     return round_up(sizeof(double) * (size_t)s->B * s->H * s->N);
 }
 
-int mar_attn_full(const mar_shape *s, const void *Q, const void *K, const void *V, void *O,
-                  float scale, const int32_t *gen_idx, int32_t G, float *score_out, float *lse_out,
-                  void *workspace, size_t workspace_bytes, uint32_t *d_status, mar_stream_t stream) {
+// Full attention, optionally with the layer-2 score and, when `select`, the top-K refresh
+// set and active set built on it.
+static int attn_full_core(const mar_shape *s, const void *Q, const void *K, const void *V, void *O, float scale,
+                          const int32_t *gen_idx, int32_t G, float *score_out, float *lse_out, void *workspace,
+                          size_t workspace_bytes, uint32_t *d_status, mar_stream_t stream, bool select,
+                          const int32_t *exclude_idx, int32_t E, int32_t Ksel, int32_t *out_idx,
+                          int32_t *active_out) {
     int rc = check_shape(s);
     if (rc != MAR_OK) return rc;
     if (s->B == 0 || s->H == 0 || s->N == 0) return MAR_OK;
@@ -94,6 +98,14 @@ int mar_attn_full(const mar_shape *s, const void *Q, const void *K, const void *
     const bool want_score = score_out != nullptr;
     if (want_score && (G <= 0 || !gen_idx)) return MAR_ERR_ARG;
     if (want_score && mar::score_smem_bytes(s->N, s->d) > 220 * 1024) return MAR_ERR_SHAPE;
+    if (select) {
+        if (!want_score || E < 0 || Ksel < 0) return MAR_ERR_ARG;
+        if (s->N > 4096) return MAR_ERR_SHAPE;
+        if (E > s->N || Ksel > s->N - E) return MAR_ERR_ARG;
+        if (E > 0 && !exclude_idx) return MAR_ERR_ARG;
+        if (!out_idx && !active_out && Ksel > 0) return MAR_ERR_ARG;
+        if (!aligned4(out_idx) || !aligned4(active_out)) return MAR_ERR_ALIGN;
+    }
     const size_t need = mar_attn_full_workspace_bytes(s, G, want_score);
     if (need && (!workspace || workspace_bytes < need ||
                  (reinterpret_cast<uintptr_t>(workspace) % kWsAlign)))
@@ -119,8 +131,30 @@ int mar_attn_full(const mar_shape *s, const void *Q, const void *K, const void *
         sp.scale = p.scale;
         e = mar::launch_score(sp, st);
         if (e != cudaSuccess) return cuda_fail(e);
+        if (select && (out_idx || active_out)) {
+            mar::TopkParams tp{};
+            tp.score = score_out; tp.exclude = exclude_idx; tp.out = out_idx; tp.active = active_out;
+            tp.status = d_status; tp.B = s->B; tp.N = s->N; tp.E = E; tp.K = Ksel;
+            e = mar::launch_topk(tp, st);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
     }
     return MAR_OK;
+}
+
+int mar_attn_full(const mar_shape *s, const void *Q, const void *K, const void *V, void *O,
+                  float scale, const int32_t *gen_idx, int32_t G, float *score_out, float *lse_out,
+                  void *workspace, size_t workspace_bytes, uint32_t *d_status, mar_stream_t stream) {
+    return attn_full_core(s, Q, K, V, O, scale, gen_idx, G, score_out, lse_out, workspace, workspace_bytes,
+                          d_status, stream, false, nullptr, 0, 0, nullptr, nullptr);
+}
+
+int mar_attn_full_select(const mar_shape *s, const void *Q, const void *K, const void *V, void *O, float scale,
+                         const int32_t *gen_idx, int32_t G, const int32_t *exclude_idx, int32_t E, int32_t Ksel,
+                         float *score_out, int32_t *out_idx, int32_t *active_out, float *lse_out,
+                         void *workspace, size_t workspace_bytes, uint32_t *d_status, mar_stream_t stream) {
+    return attn_full_core(s, Q, K, V, O, scale, gen_idx, G, score_out, lse_out, workspace, workspace_bytes,
+                          d_status, stream, true, exclude_idx, E, Ksel, out_idx, active_out);
 }
 
 static int rows_common(const mar_shape *s, int32_t A, int n, const void *const *src, void *const *dst,

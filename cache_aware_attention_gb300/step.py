@@ -17,8 +17,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (mar_attn_cache_aware, mar_attn_full, mar_attn_full_refresh, mar_attn_full_workspace_bytes,
-               mar_kv_gather, mar_refresh_topk, mar_refresh_topk_pairs)
+from . import (mar_attn_cache_aware, mar_attn_full, mar_attn_full_refresh, mar_attn_full_select,
+               mar_attn_full_workspace_bytes, mar_kv_gather, mar_refresh_topk_pairs)
 
 REFRESH_PERIOD = 3
 
@@ -101,11 +101,15 @@ class DecodeStep:
         if A > self.a_max:
             raise ValueError(f"active set of {A} exceeds a_max = {self.a_max}")
         act = self.active(A)
-        mar_attn_full(Q2, K2, V2, self.O2, gen_idx=gen, score_out=self.score, workspace=self.workspace,
-                      status=self.status, stream=stream)
-        select = mar_refresh_topk_pairs if self.shared_pairs else mar_refresh_topk
-        select(self.score, exclude, K, out_idx=self.refresh_set(K), active_out=act, status=self.status,
-               stream=stream)
+        if self.shared_pairs:
+            mar_attn_full(Q2, K2, V2, self.O2, gen_idx=gen, score_out=self.score, workspace=self.workspace,
+                          status=self.status, stream=stream)
+            mar_refresh_topk_pairs(self.score, exclude, K, out_idx=self.refresh_set(K), active_out=act,
+                                   status=self.status, stream=stream)
+        else:
+            # layer 2: attention, score, refresh set and active set
+            mar_attn_full_select(Q2, K2, V2, gen, exclude, K, self.score, O=self.O2, out_idx=self.refresh_set(K),
+                                 active_out=act, workspace=self.workspace, status=self.status, stream=stream)
         return self.cached_layer(A, layer3, cache, stream=stream)
 
     def cached_layer(self, A: int, layer3, cache, stream=None):

@@ -119,6 +119,21 @@ int mar_attn_full(const mar_shape *shape, const void *Q, const void *K, const vo
                   size_t workspace_bytes, uint32_t *d_status, mar_stream_t stream);
 
 /*
+ * mar_attn_full_select -- the layer-2 call of a cached step: full attention, the
+ * head-averaged score and, on it, the refresh set and the active set.
+ *
+ * [M] Key Design 1: exactly mar_attn_full (with score_out) followed by
+ * mar_refresh_topk(score_out, exclude_idx, E, Ksel, out_idx, active_out), issued as
+ * one call (the same launches and values).
+ *  Arguments as for mar_attn_full and mar_refresh_topk; score_out is required.
+ */
+int mar_attn_full_select(const mar_shape *shape, const void *Q, const void *K, const void *V,
+                         void *O, float scale, const int32_t *gen_idx, int32_t G,
+                         const int32_t *exclude_idx, int32_t E, int32_t Ksel, float *score_out,
+                         int32_t *out_idx, int32_t *active_out, float *lse_out, void *workspace,
+                         size_t workspace_bytes, uint32_t *d_status, mar_stream_t stream);
+
+/*
  * mar_attn_full_refresh -- full attention of a full-refresh step together with the
  * full cache overwrite of that layer.
  *

@@ -141,3 +141,16 @@ def test_next_rows_validation(lib):
     assert lib.mar_refresh_topk_pairs(2, 4097, FAKE, FAKE, 1, 1, FAKE, None, None, None) == -2
     assert lib.mar_refresh_topk_pairs(2, 10, FAKE, FAKE, 5, 6, FAKE, None, None, None) == -1   # K > N - E
     assert lib.mar_refresh_topk_pairs(2, 10, FAKE, FAKE, 2, 3, None, None, None, None) == -1   # no output
+
+
+def test_attn_full_select_validation(lib):
+    need = lib.mar_attn_full_workspace_bytes(_shape(), 4, 1)
+    def call(score=FAKE, G=4, gen=FAKE, excl=FAKE, E=8, K=4, out=FAKE, act=None, shape=None):
+        return lib.mar_attn_full_select(shape or _shape(), FAKE, FAKE + 256, FAKE + 512, FAKE + 768, 0.0, gen, G,
+                                        excl, E, K, score, out, act, None, FAKE + 4096, need, None, None)
+    assert call(score=None) == -1                   # the score is required
+    assert call(K=57) == -1                         # K > N - E
+    assert call(excl=None) == -1                    # E > 0 without exclusions
+    assert call(out=None) == -1                     # nowhere to write the selection
+    assert call(out=FAKE + 2) == -4                 # misaligned
+    assert call(shape=_shape(N=5000)) == -2         # top-K limit

@@ -358,6 +358,50 @@ def test_score_shapes(B, H, N, d, dtype, G):
     assert rel.max() < 1e-6, f"score relative error {rel.max():.3g}"
 
 
+@pytest.mark.parametrize("B,H,N,d,G,E,K", [
+    (8, 12, 320, 64, 4, 8, 32),       # MAR-B head shape
+    (2, 16, 1088, 80, 6, 12, 64),     # 512 px shape
+    (2, 20, 130, 64, 3, 6, 10),       # more heads than a cluster: two-kernel score
+    (3, 4, 200, 64, 2, 0, 7),         # no exclusions
+    (2, 2, 64, 32, 1, 2, 0),          # K = 0: only the exclusions are copied
+])
+def test_attn_full_select_equals_full_then_topk(B, H, N, d, G, E, K):
+    t = torch.bfloat16 if d != 32 else torch.float32
+    Q, Kt, V = (_rand((B, H, N, d), 560 + i, t) for i in range(3))
+    pos = workloads.distinct_positions(B, G + E, 0, N, 563).to(DEV)
+    gen = pos[:, :G].contiguous()
+    excl = pos[:, G:G + E].contiguous() if E else None
+    score = torch.empty(B, N, dtype=torch.float32, device=DEV)
+    R = torch.empty(B, K, dtype=torch.int32, device=DEV)
+    act = torch.empty(B, E + K, dtype=torch.int32, device=DEV)
+    st = _status()
+    O = mar.mar_attn_full_select(Q, Kt, V, gen, excl, K, score, out_idx=R, active_out=act, status=st)
+    assert mar.mar_status_read(st) == 0
+    # the same call pair, separately
+    O2 = mar.mar_attn_full(Q, Kt, V, gen_idx=gen, score_out=(score2 := torch.empty_like(score)))
+    assert torch.equal(O, O2) and torch.equal(score, score2)
+    ex_np = excl.cpu().numpy() if E else np.zeros((B, 0), np.int32)
+    ref = oracle.topk(score.cpu().numpy().astype(np.float64), ex_np, K)
+    if K:
+        np.testing.assert_array_equal(R.cpu().numpy(), ref)
+    np.testing.assert_array_equal(act.cpu().numpy(), np.concatenate([ex_np, ref], 1))
+
+
+def test_attn_full_select_reports_bad_exclusion():
+    B, H, N, d = 2, 12, 320, 64
+    Q, Kt, V = (_rand((B, H, N, d), 570 + i, torch.bfloat16) for i in range(3))
+    gen = workloads.distinct_positions(B, 4, 0, N, 571).to(DEV)
+    excl = gen.clone()
+    excl[1, 0] = -3
+    score = torch.empty(B, N, dtype=torch.float32, device=DEV)
+    R = torch.empty(B, 8, dtype=torch.int32, device=DEV)
+    st = _status()
+    mar.mar_attn_full_select(Q, Kt, V, gen, excl, 8, score, out_idx=R, status=st)
+    assert mar.mar_status_read(st) & mar.MAR_STATUS_INDEX_RANGE
+    np.testing.assert_array_equal(R[:1].cpu().numpy(),
+                                  oracle.topk(score[:1].cpu().numpy().astype(np.float64), gen[:1].cpu().numpy(), 8))
+
+
 @pytest.mark.parametrize("G,d", [(3, 64), (3, 80)])
 def test_score_reports_bad_generating_position(G, d):
     # an out-of-range generating position is reported and left out of the score
