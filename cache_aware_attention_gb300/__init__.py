@@ -19,8 +19,9 @@ from . import _build
 
 __all__ = [
     "MarError", "MarShape", "load", "library_path", "mar_attn_full", "mar_attn_full_workspace_bytes",
-    "mar_attn_full_noalloc",
-    "mar_attn_cache_aware", "mar_kv_scatter", "mar_kv_gather", "mar_refresh_topk",
+    "mar_attn_full_noalloc", "mar_attn_full_refresh", "mar_attn_full_select",
+    "mar_attn_cache_aware", "mar_attn_cache_aware_gather", "mar_kv_scatter", "mar_kv_gather",
+    "mar_refresh_topk", "mar_refresh_topk_pairs", "mar_token_cosine", "mar_select_recompute",
     "mar_cfg_residual", "mar_status_read", "mar_error_string", "mar_version",
     "MAR_F32", "MAR_BF16", "MAR_CFG_APPLY", "MAR_CFG_UPDATE",
     "MAR_STATUS_INDEX_RANGE", "MAR_STATUS_INDEX_DUP",
@@ -72,6 +73,7 @@ def load(path: str | None = None):
         "mar_attn_full_select": ([SP, P, P, P, P, F, P, I32, P, I32, I32, P, P, P, P, P, SZ, P, P], ctypes.c_int),
         "mar_attn_cache_aware_workspace_bytes": ([SP, I32], SZ),
         "mar_attn_cache_aware": ([SP, I32, P, P, P, P, P, P, P, F, P, I32, P, SZ, P, P], ctypes.c_int),
+        "mar_attn_cache_aware_gather": ([SP, I32, P, P, P, P, P, P, P, F, P, I32, P, P], ctypes.c_int),
         "mar_kv_scatter": ([SP, I32, P, P, P, P, P, P, P], ctypes.c_int),
         "mar_kv_gather": ([SP, I32, I32, P, P, P, P, P], ctypes.c_int),
         "mar_refresh_topk": ([I32, I32, P, P, I32, I32, P, P, P, P], ctypes.c_int),
@@ -231,6 +233,23 @@ def mar_attn_cache_aware(Q_A, K_A, V_A, K_cache, V_cache, active_idx, O_A=None, 
                                   _ptr(lse_out), int(bool(fuse_scatter)), _ptr(workspace), wb,
                                   _ptr(status), _stream(stream))
     _check("mar_attn_cache_aware", rc)
+    return O_A
+
+
+def mar_attn_cache_aware_gather(Q, K, V, K_cache, V_cache, active_idx, O_A=None, scale: float = 0.0,
+                                lse_out=None, fuse_scatter: bool = False, status=None, stream=None):
+    """Cache-aware attention of the active rows of the fresh Q/K/V [B,H,N,d], read in place
+    through active_idx [B,A] (gather, attention and optional cache update in one launch);
+    returns O_A [B,H,A,d]."""
+    lib = load()
+    A = int(active_idx.shape[1])
+    s = _shape(Q)
+    if O_A is None:
+        O_A = torch.empty(Q.shape[0], Q.shape[1], A, Q.shape[3], dtype=Q.dtype, device=Q.device)
+    rc = lib.mar_attn_cache_aware_gather(ctypes.byref(s), A, _ptr(Q), _ptr(K), _ptr(V), _ptr(K_cache),
+                                         _ptr(V_cache), _ptr(active_idx), _ptr(O_A), float(scale),
+                                         _ptr(lse_out), int(bool(fuse_scatter)), _ptr(status), _stream(stream))
+    _check("mar_attn_cache_aware_gather", rc)
     return O_A
 
 

@@ -157,6 +157,34 @@ int mar_attn_full_select(const mar_shape *s, const void *Q, const void *K, const
                           d_status, stream, true, exclude_idx, E, Ksel, out_idx, active_out);
 }
 
+int mar_attn_cache_aware_gather(const mar_shape *s, int32_t A, const void *Q, const void *K, const void *V,
+                                void *K_cache, void *V_cache, const int32_t *active_idx, void *O_A, float scale,
+                                float *lse_out, int32_t fuse_scatter, uint32_t *d_status, mar_stream_t stream) {
+    int rc = check_shape(s);
+    if (rc != MAR_OK) return rc;
+    if (A < 0 || A > s->N) return MAR_ERR_ARG;
+    if (A == 0 || s->B == 0 || s->H == 0) return MAR_OK;
+    if (!Q || !K || !V || !K_cache || !V_cache || !active_idx || !O_A) return MAR_ERR_ARG;
+    // the cache is written (fused scatter) while the fresh tensors are read: distinct buffers
+    if (K_cache == K || V_cache == V || K_cache == V_cache || K_cache == Q || V_cache == Q) return MAR_ERR_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(K_cache) || !aligned16(V_cache) ||
+        !aligned16(O_A) || !aligned4(lse_out) || !aligned4(active_idx))
+        return MAR_ERR_ALIGN;
+    if (s->N > kMaxCacheN) return MAR_ERR_SHAPE;
+    if ((long long)s->B * s->H * s->N > 0x7fffffffLL) return MAR_ERR_SHAPE;  // gather row coordinates
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+    mar::AttnParams p{};
+    p.Q = Q; p.Kd = K; p.Vd = V; p.Kc = K_cache; p.Vc = V_cache; p.idx = active_idx;
+    p.O = O_A; p.lse = lse_out; p.status = d_status;
+    p.B = s->B; p.H = s->H; p.N = s->N; p.d = s->d;
+    p.nq = A; p.n_dense = A; p.A = A; p.fuse_scatter = fuse_scatter ? 1 : 0; p.fresh = 1;
+    p.scale = resolve_scale(scale, s->d);
+    cudaError_t e = (s->dtype == MAR_BF16) ? mar::launch_attn_bf16(p, st) : mar::launch_attn_f32(p, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return MAR_OK;
+}
+
 static int rows_common(const mar_shape *s, int32_t A, int n, const void *const *src, void *const *dst,
                        const int32_t *idx, int scatter, uint32_t *d_status, mar_stream_t stream);
 

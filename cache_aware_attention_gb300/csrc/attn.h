@@ -14,6 +14,8 @@ namespace mar {
 // Full attention: Kd/Vd = K/V with n_dense = N, idx = nullptr; with store_kv the launch
 // also copies K/V into Kc/Vc (the full cache refresh).
 // Cache-aware attention: Kd/Vd = K_A/V_A with n_dense = A, idx = active positions.
+// With `fresh` set, Q/Kd/Vd are the whole fresh tensors [B*H, N, d] and row a of the
+// active set is read at row idx[b, a] (the active gather folded into the launch).
 struct AttnParams {
     const void *Q;      // [B*H, nq, d]
     const void *Kd;     // [B*H, n_dense, d]
@@ -28,9 +30,21 @@ struct AttnParams {
     int B, H, N, d;
     int nq, n_dense, A;
     int fuse_scatter;
+    int fresh;          // cache-aware only: Q/Kd/Vd are [B*H, N, d], active row a at idx[b, a]
     int store_kv;       // full attention only: Kc/Vc := Kd/Vd (tcgen05 kernel only)
     float scale;        // softmax scale
 };
+
+#ifdef __CUDACC__
+// Row of Q/Kd/Vd holding dense row a of (b, h): a itself, or with `fresh` the active
+// position idx[b, a] of the whole tensor (an out-of-range position reads row 0 of the slab;
+// the bitmap build reports it).
+__device__ __forceinline__ int64_t dense_row(const AttnParams &p, int bh, int b, int a, int rows) {
+    if (!p.fresh) return (int64_t)bh * rows + a;
+    const int pos = p.idx[(int64_t)b * p.A + a];
+    return (int64_t)bh * p.N + ((pos >= 0 && pos < p.N) ? pos : 0);
+}
+#endif
 
 // Launchers. Return the cudaError_t of the launch.
 cudaError_t launch_attn_f32(const AttnParams &p, cudaStream_t s);

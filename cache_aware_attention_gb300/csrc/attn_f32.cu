@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const AttnParams 
                 int a = t / vec, c = t % vec;
                 int pos = p.idx[(int64_t)b * p.A + a];
                 if (pos < 0 || pos >= p.N) continue;
-                const int64_t src = ((int64_t)bh * p.n_dense + a) * d + 4 * c;
+                const int64_t src = dense_row(p, bh, b, a, p.n_dense) * d + 4 * c;
                 const int64_t dst = ((int64_t)bh * p.N + pos) * d + 4 * c;
                 *reinterpret_cast<float4 *>(Kc + dst) = *reinterpret_cast<const float4 *>(Kd + src);
                 *reinterpret_cast<float4 *>(Vc + dst) = *reinterpret_cast<const float4 *>(Vd + src);
@@ -54,11 +54,12 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const AttnParams 
     const int i = qt * kWarps + warp;
     if (i >= p.nq) return;
 
+    const int64_t qrow = dense_row(p, bh, b, i, p.nq);
     float q[MAXC], o[MAXC];
 #pragma unroll
     for (int k = 0; k < MAXC; ++k) {
         int c = lane + 32 * k;
-        q[k] = (c < d) ? Q[((int64_t)bh * p.nq + i) * d + c] : 0.f;
+        q[k] = (c < d) ? Q[qrow * d + c] : 0.f;
         o[k] = 0.f;
     }
     float m = -INFINITY, l = 0.f;
@@ -66,8 +67,9 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const AttnParams 
     for (int t = 0; t < n_keys; ++t) {
         const float *kr, *vr;
         if (t < p.n_dense) {
-            kr = Kd + ((int64_t)bh * p.n_dense + t) * d;
-            vr = Vd + ((int64_t)bh * p.n_dense + t) * d;
+            const int64_t r = dense_row(p, bh, b, t, p.n_dense);
+            kr = Kd + r * d;
+            vr = Vd + r * d;
         } else {
             int pos = cached[t - p.n_dense];
             kr = Kc + ((int64_t)bh * p.N + pos) * d;

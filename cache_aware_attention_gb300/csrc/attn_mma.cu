@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(const AttnParams p) 
                 int a = t / KCH, c = t % KCH;
                 int pos = p.idx[(int64_t)b * p.A + a];
                 if (pos < 0 || pos >= p.N) continue;
-                const int64_t src = ((int64_t)bh * p.n_dense + a) * D + 8 * c;
+                const int64_t src = dense_row(p, bh, b, a, p.n_dense) * D + 8 * c;
                 const int64_t dst = ((int64_t)bh * p.N + pos) * D + 8 * c;
                 *reinterpret_cast<uint4 *>(Kc + dst) = *reinterpret_cast<const uint4 *>(Kd + src);
                 *reinterpret_cast<uint4 *>(Vc + dst) = *reinterpret_cast<const uint4 *>(Vd + src);
@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(const AttnParams p) 
     // Query tile: rows past nq are zero-filled.
     for (int c = tid; c < BM * KCH; c += kThreads) {
         int r = c / KCH, ch = c % KCH, row = q0 + r;
-        const bf16 *src = Q + ((int64_t)bh * p.nq + (row < p.nq ? row : 0)) * D + 8 * ch;
+        const bf16 *src = Q + dense_row(p, bh, b, row < p.nq ? row : 0, p.nq) * D + 8 * ch;
         cp_async16(sQ + r * LD + 8 * ch, src, row < p.nq ? 16 : 0);
     }
     auto load_kv = [&](int blk, int buf) {
@@ -87,8 +87,9 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(const AttnParams p) 
             const bf16 *ks = Kd, *vs = Vd;
             int bytes = 16;
             if (t < p.n_dense) {
-                ks = Kd + ((int64_t)bh * p.n_dense + t) * D + 8 * ch;
-                vs = Vd + ((int64_t)bh * p.n_dense + t) * D + 8 * ch;
+                const int64_t r = dense_row(p, bh, b, t, p.n_dense);
+                ks = Kd + r * D + 8 * ch;
+                vs = Vd + r * D + 8 * ch;
             } else if (t < n_keys) {
                 int pos = sList[t - p.n_dense];
                 ks = Kc + ((int64_t)bh * p.N + pos) * D + 8 * ch;

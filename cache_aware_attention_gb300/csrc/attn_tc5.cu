@@ -28,7 +28,9 @@
 //   warp 7     PV issuer (one elected lane): O += P_g V_g  (M=128, N=d, K=64, P from
 //              TMEM, V MN-major), as soon as P_g is written; it releases the K/V stage
 //   warp 6     index warp: bitmap of the active positions of each tile (double-
-//              buffered) and the fused cache scatter.
+//              buffered), the fused cache scatter and, when the active rows are read in
+//              place from the whole fresh tensors, the copies of those rows into the Q
+//              buffer and the dense-block stages (which the producer hands over).
 // g numbers the key blocks of a CTA across its tiles; every ring (stages, S/P buffers,
 // Q buffers, bitmaps) is indexed by g or by the tile count, and every barrier is waited
 // one phase at a time, in order, so parity waits are exact.
@@ -91,12 +93,16 @@ enum Bar {
     O_DONE = 10,     // [kSB] PV of block g -> O_DONE[g % kSB]
     BM_FULL = 13,    // [2]
     BM_EMPTY = 15,   // [2]
-    KV_FULL = 17     // [S], then KV_EMPTY [S]
+    O_STAGED = 17,   // [2] the tile's normalised O is in its Q buffer (one arrival per softmax warp)
+    DENSE_DONE = 19, // [S <= 4] fresh mode: the index warp is done reading a dense-block stage
+    DENSE_GO = 23,   // [S] fresh mode: the producer hands a free stage for a dense block to it
+    KV_FULL = 27     // [S], then KV_EMPTY [S]
 };
 
 template <int D>
 struct Tc5Params {
     CUtensorMap mQa, mQb;    // 3-D [BH, nq, D]: box {64,128,1} (SW128) / {16,128,1} (SW32)
+    CUtensorMap mOa, mOb;    // O, the same layout and boxes (tile stores from the staged Q buffer)
     CUtensorMap mKa, mKb;    // 3-D [BH, n_dense, D], box {64|16, 64, 1}: all rows / active rows
     CUtensorMap mVa, mVb;
     CUtensorMap mKca, mKcb;  // cache [BH, N, D], box {64|16, 64, 1}: read (cache-aware) or
@@ -145,6 +151,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             mbar_init(&bars[Q_EMPTY + i], 1);
             mbar_init(&bars[BM_FULL + i], 1);
             mbar_init(&bars[BM_EMPTY + i], 4);
+            mbar_init(&bars[O_STAGED + i], 4);
         }
         for (int i = 0; i < SB; ++i) {
             mbar_init(&bars[S_FULL + i], 1);
@@ -152,6 +159,8 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             mbar_init(&bars[O_DONE + i], 1);
         }
         for (int i = 0; i < S; ++i) {
+            mbar_init(&bars[DENSE_GO + i], 1);
+            mbar_init(&bars[DENSE_DONE + i], 1);
             mbar_init(&bars[KV_FULL + i], 1);
             mbar_init(&kv_empty[i], 1);
         }
@@ -189,20 +198,52 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                 pend_g = -1;
                 return true;
             };
+            // O of tile t is staged by the softmax warps in Q buffer t & 1; it is stored to
+            // global memory by TMA from there before that buffer takes the Q of tile t + 2 (or
+            // after the last tile), and the buffer is reloaded only once the store has read it.
+            // (In fresh mode the index warp owns the Q buffers and does this.)
+            auto store_o = [&](int t) -> bool {
+                if (!mbar_wait(&bars[O_STAGED + (t & 1)], (t >> 1) & 1, p.status, abort_flag)) return false;
+                const int tt = (int)blockIdx.x + t * (int)gridDim.x;
+                const int tbh = tt / nqt, tq0 = (tt % nqt) * BM;
+                const unsigned char *src = sm + C::oQ + (t & 1) * C::kQBytes;
+                tma_store_3d(&P.mOa, 0, tq0, tbh, src);
+                if constexpr (C::DB > 0) tma_store_3d(&P.mOb, 64, tq0, tbh, src + C::kQa);
+                bulk_commit_group();
+                bulk_wait_group_read<0>();
+                return true;
+            };
             bool ok = true;
+            uint32_t done_phase = 0;  // fresh mode: bit st = parity of the next DENSE_DONE[st] phase
             for (int it = 0; ok && it < my_tiles; ++it) {
                 const int tile = (int)blockIdx.x + it * (int)gridDim.x;
                 const int bh = tile / nqt, q0 = (tile % nqt) * BM;
                 const bool store_tile = P.store && q0 == 0;
                 const int qb = it & 1;
-                if (!(ok = mbar_wait(&bars[Q_EMPTY + qb], ((it >> 1) & 1) ^ 1, p.status, abort_flag))) break;
                 unsigned char *sq = sm + C::oQ + qb * C::kQBytes;
-                mbar_arrive_expect_tx(&bars[Q_FULL + qb], C::kQa + C::kQb);
-                tma_load_3d(sq, &P.mQa, 0, q0, bh, &bars[Q_FULL + qb]);
-                if constexpr (C::DB > 0) tma_load_3d(sq + C::kQa, &P.mQb, 64, q0, bh, &bars[Q_FULL + qb]);
+                if (!p.fresh) {
+                    if (it >= 2 && !(ok = store_o(it - 2))) break;  // the buffer still holds O of tile it - 2
+                    if (!(ok = mbar_wait(&bars[Q_EMPTY + qb], ((it >> 1) & 1) ^ 1, p.status, abort_flag))) break;
+                    mbar_arrive_expect_tx(&bars[Q_FULL + qb], C::kQa + C::kQb);
+                    tma_load_3d(sq, &P.mQa, 0, q0, bh, &bars[Q_FULL + qb]);
+                    if constexpr (C::DB > 0) tma_load_3d(sq + C::kQa, &P.mQb, 64, q0, bh, &bars[Q_FULL + qb]);
+                }
                 for (int j = 0; j < nblk; ++j) {
                     const int g = it * nblk + j, st = g % S;
                     if (!(ok = mbar_wait(&kv_empty[st], ((g / S) & 1) ^ 1, p.status, abort_flag))) break;
+                    if (p.fresh) {
+                        // a stage last used by a dense block is free once the index warp has also
+                        // finished reading it (the fused scatter)
+                        if (g >= S && (g - S) % nblk < nd) {
+                            if (!(ok = mbar_wait(&bars[DENSE_DONE + st], (done_phase >> st) & 1, p.status, abort_flag)))
+                                break;
+                            done_phase ^= 1u << st;
+                        }
+                        if (j < nd) {  // the index warp fills this stage and signals it
+                            mbar_arrive(&bars[DENSE_GO + st]);
+                            continue;
+                        }
+                    }
                     if (P.store) bulk_wait_group_read<S - 2>();  // the store of block g - S is done reading
                     unsigned char *stg = sm + C::oStage + st * C::kStageBytes;
                     uint64_t *fb = &bars[KV_FULL + st];
@@ -229,8 +270,12 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             if (P.store) {
                 if (ok) store_pending();
                 bulk_commit_group();
-                bulk_wait_group<0>();  // every store complete before the CTA exits
             }
+            for (int t = my_tiles - 2; ok && !p.fresh && t < my_tiles; ++t)
+                if (t >= 0) ok = store_o(t);
+            // every store has read its shared-memory source before the CTA exits (the writes
+            // themselves are visible to later launches at grid completion)
+            bulk_wait_group_read<0>();
         }
         __syncwarp();
     } else if (warp == 5) {
@@ -300,30 +345,167 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
         __syncwarp();
     } else if (warp == 6) {
         // ------------------------------------------------------------ index warp
-        if (P.gather) {
-            for (int it = 0; it < my_tiles; ++it) {
+        // Fresh mode: the active rows of the tile's queries and of its dense key blocks are
+        // copied here from the whole fresh tensors (rows bh * N + idx[b, a]), 16 bytes per
+        // lane per copy, into the same swizzled layouts the TMA boxes produce: row r of a
+        // 64-column part at r * 128 with its chunk c at (c ^ (r & 7)) * 16, the 16 tail
+        // columns of d = 80 at r * 32 with chunk c at (c ^ ((r >> 2) & 1)) * 16. Rows past the
+        // active set (and rows at out-of-range positions) are zero-filled. Each lane waits for
+        // its own copies and fences them for the tensor cores before lane 0 signals the barrier.
+        const bf16 *gQ = static_cast<const bf16 *>(p.Q);
+        const bf16 *gK = static_cast<const bf16 *>(p.Kd);
+        const bf16 *gV = static_cast<const bf16 *>(p.Vd);
+        // rows a0 .. a0 + rows - 1 of the active set (rows <= 128, a multiple of 32) of one or
+        // two tensors into part a at da[n] and tail part at db[n]
+        auto copy_rows = [&](const bf16 *const *src, unsigned char *const *da, unsigned char *const *db, int n,
+                             int a0, int rows, int64_t slab, const int32_t *ix) {
+            int pr[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int a = a0 + 32 * k + lane;
+                const int pos = (32 * k < rows && a < p.A) ? __ldg(ix + a) : -1;
+                pr[k] = (pos >= 0 && pos < p.N) ? pos : -1;
+            }
+            for (int i = 0; i < rows / 4; ++i) {  // four rows per pass: 8 lanes per row
+                const int r = 4 * i + (lane >> 3), c = lane & 7, sel = i >> 3;
+                const int pos = __shfl_sync(0xffffffffu, sel == 0 ? pr[0] : sel == 1 ? pr[1] : sel == 2 ? pr[2] : pr[3],
+                                            r & 31);
+                const int64_t off = (slab + (pos < 0 ? 0 : pos)) * D + 8 * c;
+                const uint32_t so = (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+                for (int t = 0; t < n; ++t) cp_async16(da[t] + so, src[t] + off, pos < 0 ? 0 : 16);
+            }
+            if constexpr (C::DB > 0) {
+                for (int i = 0; i < rows / 16; ++i) {  // sixteen rows per pass: 2 lanes per row
+                    const int r = 16 * i + (lane >> 1), c = lane & 1, sel = i >> 1;
+                    const int pos = __shfl_sync(0xffffffffu,
+                                                sel == 0 ? pr[0] : sel == 1 ? pr[1] : sel == 2 ? pr[2] : pr[3], r & 31);
+                    const int64_t off = (slab + (pos < 0 ? 0 : pos)) * D + 64 + 8 * c;
+                    const uint32_t so = (uint32_t)(r * 32 + ((c ^ ((r >> 2) & 1)) << 4));
+                    for (int t = 0; t < n; ++t) cp_async16(db[t] + so, src[t] + off, pos < 0 ? 0 : 16);
+                }
+            }
+        };
+        // Fused scatter in fresh mode, from the stage just filled: the real rows of dense block
+        // a0 .. a0 + 63 go to the cache rows at their positions (K and V). The producer refills
+        // the stage only after DENSE_DONE, which follows these reads.
+        bf16 *gKc = static_cast<bf16 *>(p.Kc);
+        bf16 *gVc = static_cast<bf16 *>(p.Vc);
+        auto scatter_stage = [&](const unsigned char *stg, int a0, int64_t slab, const int32_t *ix) {
+            const int nr = min(BN, p.A - a0);
+            for (int i = 0; i < (nr + 3) / 4; ++i) {
+                const int r = 4 * i + (lane >> 3), c = lane & 7;
+                const int pos = r < nr ? __ldg(ix + a0 + r) : -1;
+                if (pos < 0 || pos >= p.N) continue;
+                const uint32_t so = (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+                const int64_t off = (slab + pos) * D + 8 * c;
+                *reinterpret_cast<uint4 *>(gKc + off) = *reinterpret_cast<const uint4 *>(stg + C::sKa + so);
+                *reinterpret_cast<uint4 *>(gVc + off) = *reinterpret_cast<const uint4 *>(stg + C::sVa + so);
+            }
+            if constexpr (C::DB > 0) {
+                for (int i = 0; i < (nr + 15) / 16; ++i) {
+                    const int r = 16 * i + (lane >> 1), c = lane & 1;
+                    const int pos = r < nr ? __ldg(ix + a0 + r) : -1;
+                    if (pos < 0 || pos >= p.N) continue;
+                    const uint32_t so = (uint32_t)(r * 32 + ((c ^ ((r >> 2) & 1)) << 4));
+                    const int64_t off = (slab + pos) * D + 64 + 8 * c;
+                    *reinterpret_cast<uint4 *>(gKc + off) = *reinterpret_cast<const uint4 *>(stg + C::sKb + so);
+                    *reinterpret_cast<uint4 *>(gVc + off) = *reinterpret_cast<const uint4 *>(stg + C::sVb + so);
+                }
+            }
+        };
+        auto land = [&]() {  // this lane's copies complete and visible to the tensor cores
+            cp_async_commit();
+            cp_async_wait<0>();
+            fence_proxy_async_smem();
+            __syncwarp();
+        };
+        // the bitmap of tile it's active positions (double-buffered; handed to the softmax
+        // warps when the tile has cache blocks), with the positions checked
+        auto build_bitmap = [&](int it, int b) -> bool {
+            const int bb = it & 1;
+            uint32_t *bm = bitmaps + bb * bm_words;
+            if (nc > 0 && !mbar_wait(&bars[BM_EMPTY + bb], ((it >> 1) & 1) ^ 1, p.status, abort_flag)) return false;
+            for (int w = lane; w < bm_words; w += 32) bm[w] = 0u;
+            __syncwarp();
+            uint32_t bad = 0;
+            for (int a = lane; a < p.A; a += 32) {
+                const int pos = p.idx[(int64_t)b * p.A + a];
+                if (pos < 0 || pos >= p.N) {
+                    bad |= MAR_STATUS_INDEX_RANGE;
+                    continue;
+                }
+                const uint32_t old = atomicOr(&bm[pos >> 5], 1u << (pos & 31));
+                if (old & (1u << (pos & 31))) bad |= MAR_STATUS_INDEX_DUP;
+            }
+            if (bad) report(p.status, bad);
+            __syncwarp();
+            if (nc > 0 && lane == 0) mbar_arrive(&bars[BM_FULL + bb]);
+            return true;
+        };
+        // fresh mode: this warp owns the Q buffers, so it also stores each tile's staged O
+        auto store_o6 = [&](int t) -> bool {
+            if (!mbar_wait(&bars[O_STAGED + (t & 1)], (t >> 1) & 1, p.status, abort_flag)) return false;
+            if (lane == 0) {
+                const int tt = (int)blockIdx.x + t * (int)gridDim.x;
+                const int tbh = tt / nqt, tq0 = (tt % nqt) * BM;
+                const unsigned char *src = sm + C::oQ + (t & 1) * C::kQBytes;
+                tma_store_3d(&P.mOa, 0, tq0, tbh, src);
+                if constexpr (C::DB > 0) tma_store_3d(&P.mOb, 64, tq0, tbh, src + C::kQa);
+                bulk_commit_group();
+                bulk_wait_group_read<0>();
+            }
+            __syncwarp();
+            return true;
+        };
+        if (P.gather && p.fresh) {
+            bool ok = true;
+            uint32_t go_phase = 0;  // bit st: parity of the next DENSE_GO[st] phase
+            for (int it = 0; ok && it < my_tiles; ++it) {
                 const int tile = (int)blockIdx.x + it * (int)gridDim.x;
                 const int bh = tile / nqt, qt = tile % nqt, b = bh / p.H;
-                const int bb = it & 1;
-                uint32_t *bm = bitmaps + bb * bm_words;
-                if (nc > 0) {  // with no cache blocks (A == N) nothing reads the bitmap
-                    if (!mbar_wait(&bars[BM_EMPTY + bb], ((it >> 1) & 1) ^ 1, p.status, abort_flag)) break;
-                    for (int w = lane; w < bm_words; w += 32) bm[w] = 0u;
-                    __syncwarp();
-                    uint32_t bad = 0;
-                    for (int a = lane; a < p.A; a += 32) {
-                        const int pos = p.idx[(int64_t)b * p.A + a];
-                        if (pos < 0 || pos >= p.N) {
-                            bad |= MAR_STATUS_INDEX_RANGE;
-                            continue;
-                        }
-                        const uint32_t old = atomicOr(&bm[pos >> 5], 1u << (pos & 31));
-                        if (old & (1u << (pos & 31))) bad |= MAR_STATUS_INDEX_DUP;
-                    }
-                    if (bad) report(p.status, bad);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars[BM_FULL + bb]);
+                const int qb = it & 1, q0 = qt * BM;
+                const int32_t *ix = p.idx + (int64_t)b * p.A;
+                const int64_t slab = (int64_t)bh * p.N;
+                // the buffer holds O of tile it - 2 (all of that tile's MMAs are complete)
+                if (it >= 2 && !(ok = store_o6(it - 2))) break;
+                {
+                    unsigned char *sq = sm + C::oQ + qb * C::kQBytes;
+                    unsigned char *sqb = sq + C::kQa;
+                    // whole warps of query rows (those of a warp with no real row are never read)
+                    copy_rows(&gQ, &sq, &sqb, 1, q0, min(BM, (p.nq - q0 + 31) & ~31), slab, ix);
                 }
+                for (int j = 0; j < nd; ++j) {
+                    const int g = it * nblk + j, st = g % S;
+                    if (!(ok = mbar_wait(&bars[DENSE_GO + st], (go_phase >> st) & 1, p.status, abort_flag))) break;
+                    go_phase ^= 1u << st;
+                    unsigned char *stg = sm + C::oStage + st * C::kStageBytes;
+                    const bf16 *src[2] = {gK, gV};
+                    unsigned char *da[2] = {stg + C::sKa, stg + C::sVa};
+                    unsigned char *db[2] = {stg + C::sKb, stg + C::sVb};
+                    copy_rows(src, da, db, 2, j * BN, BN, slab, ix);
+                    land();
+                    if (lane == 0) {
+                        if (j == 0) mbar_arrive(&bars[Q_FULL + qb]);
+                        mbar_arrive(&bars[KV_FULL + st]);
+                    }
+                    // the bitmap is read from the first cache block on; the positions are
+                    // checked even when there is none (A == N)
+                    if (j == 0 && !(ok = build_bitmap(it, b))) break;
+                    if (p.fuse_scatter && qt == 0) scatter_stage(stg, j * BN, slab, ix);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[DENSE_DONE + st]);
+                }
+            }
+            for (int t = my_tiles - 2; ok && t < my_tiles; ++t)
+                if (t >= 0) ok = store_o6(t);
+            if (lane == 0) bulk_wait_group_read<0>();
+        } else if (P.gather) {
+            bool ok = true;
+            for (int it = 0; ok && it < my_tiles; ++it) {
+                const int tile = (int)blockIdx.x + it * (int)gridDim.x;
+                const int bh = tile / nqt, qt = tile % nqt, b = bh / p.H;
+                // with no cache blocks (A == N) nothing reads the bitmap
+                if (nc > 0 && !(ok = build_bitmap(it, b))) break;
                 if (p.fuse_scatter && qt == 0) {
                     // Fresh K_A/V_A rows -> cache rows of the active positions. No query of
                     // this launch uses those rows (they are masked as stale).
@@ -469,29 +651,43 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             if (!(ok = mbar_wait(&bars[O_DONE + gl % SB], (gl / SB) & 1, p.status, abort_flag))) break;
             tc_fence_after();
             if (live) {
-                const int row = q0 + tid;
+                // normalised O, staged as bf16 in this tile's Q buffer (free: the tile's last S
+                // has completed) in the layout of the TMA boxes: row r of the 64-column part at
+                // r * 128 with its 16-byte chunk c at (c ^ (r & 7)) * 16 (128-byte swizzle); the
+                // 16 tail columns of d = 80 at r * 32, chunk c at (c ^ ((r >> 2) & 1)) * 16
+                // (32-byte swizzle). The producer stores the tile (rows past nq are clipped).
+                const int row = q0 + tid, r = tid;
                 const float inv = 1.f / l;
-                bf16 *Og = static_cast<bf16 *>(p.O) + ((int64_t)bh * p.nq + row) * D;
+                unsigned char *stage = sm + C::oQ + (it & 1) * C::kQBytes;
 #pragma unroll
                 for (int c0 = 0; c0 < D; c0 += 16) {
                     float o[16];
                     tmem_ld16(lane_addr(tmO, warp, c0), o);
-                    if (row < p.nq) {
-                        uint4 u0, u1;
-                        u0.x = pack_bf16x2(o[0] * inv, o[1] * inv);
-                        u0.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-                        u0.z = pack_bf16x2(o[4] * inv, o[5] * inv);
-                        u0.w = pack_bf16x2(o[6] * inv, o[7] * inv);
-                        u1.x = pack_bf16x2(o[8] * inv, o[9] * inv);
-                        u1.y = pack_bf16x2(o[10] * inv, o[11] * inv);
-                        u1.z = pack_bf16x2(o[12] * inv, o[13] * inv);
-                        u1.w = pack_bf16x2(o[14] * inv, o[15] * inv);
-                        *reinterpret_cast<uint4 *>(Og + c0) = u0;
-                        *reinterpret_cast<uint4 *>(Og + c0 + 8) = u1;
+                    uint4 u0, u1;
+                    u0.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+                    u0.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+                    u0.z = pack_bf16x2(o[4] * inv, o[5] * inv);
+                    u0.w = pack_bf16x2(o[6] * inv, o[7] * inv);
+                    u1.x = pack_bf16x2(o[8] * inv, o[9] * inv);
+                    u1.y = pack_bf16x2(o[10] * inv, o[11] * inv);
+                    u1.z = pack_bf16x2(o[12] * inv, o[13] * inv);
+                    u1.w = pack_bf16x2(o[14] * inv, o[15] * inv);
+                    if (c0 < 64) {
+                        const int c = c0 >> 3;  // chunks c, c + 1 of the row
+                        *reinterpret_cast<uint4 *>(stage + r * 128 + ((c ^ (r & 7)) << 4)) = u0;
+                        *reinterpret_cast<uint4 *>(stage + r * 128 + (((c + 1) ^ (r & 7)) << 4)) = u1;
+                    } else {
+                        unsigned char *tail = stage + C::kQa;
+                        const int sw = (r >> 2) & 1;
+                        *reinterpret_cast<uint4 *>(tail + r * 32 + ((0 ^ sw) << 4)) = u0;
+                        *reinterpret_cast<uint4 *>(tail + r * 32 + ((1 ^ sw) << 4)) = u1;
                     }
                 }
                 if (p.lse && row < p.nq) p.lse[(int64_t)bh * p.nq + row] = (m_use + log2f(l)) * kLn2;
             }
+            fence_proxy_async_smem();  // the staged rows, for the TMA store
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[O_STAGED + (it & 1)]);
             // The next tile's first PV overwrites O only after P of its first block, which
             // this warp group writes after the reads above have completed.
         }
@@ -531,9 +727,19 @@ cudaError_t launch(const AttnParams &p, cudaStream_t s) {
     P.gather = p.idx ? 1 : 0;
     const int bh = p.B * p.H;
     const uint32_t tw = D == 64 ? 64 : 16;  // tail box width (the tail maps are unused for d = 64)
-    bool ok = map3<D>(&P.mQa, p.Q, p.nq, bh, 64, BM) && map3<D>(&P.mQb, p.Q, p.nq, bh, tw, BM);
-    ok = ok && map3<D>(&P.mKa, p.Kd, p.n_dense, bh, 64, BN) && map3<D>(&P.mKb, p.Kd, p.n_dense, bh, tw, BN);
-    ok = ok && map3<D>(&P.mVa, p.Vd, p.n_dense, bh, 64, BN) && map3<D>(&P.mVb, p.Vd, p.n_dense, bh, tw, BN);
+    bool ok = map3<D>(&P.mOa, p.O, p.nq, bh, 64, BM) && map3<D>(&P.mOb, p.O, p.nq, bh, tw, BM);
+    if (p.fresh) {
+        // the index warp copies the active rows; these maps over the whole fresh tensors are
+        // only prefetched, never loaded from
+        if (!p.idx || p.nq != p.A || p.n_dense != p.A) return cudaErrorInvalidValue;
+        ok = ok && map3<D>(&P.mQa, p.Q, p.N, bh, 64, BM) && map3<D>(&P.mQb, p.Q, p.N, bh, tw, BM);
+        ok = ok && map3<D>(&P.mKa, p.Kd, p.N, bh, 64, BN) && map3<D>(&P.mKb, p.Kd, p.N, bh, tw, BN);
+        ok = ok && map3<D>(&P.mVa, p.Vd, p.N, bh, 64, BN) && map3<D>(&P.mVb, p.Vd, p.N, bh, tw, BN);
+    } else {
+        ok = ok && map3<D>(&P.mQa, p.Q, p.nq, bh, 64, BM) && map3<D>(&P.mQb, p.Q, p.nq, bh, tw, BM);
+        ok = ok && map3<D>(&P.mKa, p.Kd, p.n_dense, bh, 64, BN) && map3<D>(&P.mKb, p.Kd, p.n_dense, bh, tw, BN);
+        ok = ok && map3<D>(&P.mVa, p.Vd, p.n_dense, bh, 64, BN) && map3<D>(&P.mVb, p.Vd, p.n_dense, bh, tw, BN);
+    }
     P.store = (!P.gather && p.store_kv) ? 1 : 0;
     if (P.gather || P.store) {
         ok = ok && map3<D>(&P.mKca, p.Kc, p.N, bh, 64, BN) && map3<D>(&P.mKcb, p.Kc, p.N, bh, tw, BN);

@@ -17,8 +17,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (mar_attn_cache_aware, mar_attn_full, mar_attn_full_refresh, mar_attn_full_select,
-               mar_attn_full_workspace_bytes, mar_kv_gather, mar_refresh_topk_pairs)
+from . import (mar_attn_cache_aware, mar_attn_cache_aware_gather, mar_attn_full, mar_attn_full_refresh,
+               mar_attn_full_select, mar_attn_full_workspace_bytes, mar_kv_gather, mar_refresh_topk_pairs)
 
 REFRESH_PERIOD = 3
 
@@ -39,21 +39,24 @@ class DecodeStep:
     latency/FID trade-off of Figure 6 speak of a fixed number of active tokens per step):
     K = budget - (G + J) at each step instead of a fixed K. ``shared_pairs``: rows b and
     b + B'/2 (conditional and unconditional halves of a guidance batch) share one refresh
-    set, ranked on the sum of their scores."""
+    set, ranked on the sum of their scores. ``fused_gather``: the cache-aware layer reads its
+    active rows in place from the fresh tensors (one launch for gather, attention and cache
+    update) instead of gathering them into dense blocks first."""
 
     def __init__(self, B: int, H: int, N: int, d: int, K: int, a_max: int, dtype=torch.bfloat16,
                  device="cuda", max_gen: int | None = None, budget: int | None = None,
-                 shared_pairs: bool = False):
+                 shared_pairs: bool = False, fused_gather: bool = True):
         if shared_pairs and B % 2:
             raise ValueError("shared_pairs needs an even number of rows")
         self.B, self.H, self.N, self.d, self.K, self.a_max = B, H, N, d, K, a_max
-        self.budget, self.shared_pairs = budget, shared_pairs
+        self.budget, self.shared_pairs, self.fused_gather = budget, shared_pairs, fused_gather
         self.device = torch.device(device)
         dev, f32, i32 = self.device, torch.float32, torch.int32
         self.score = torch.empty(B, N, dtype=f32, device=dev)
         self._R = torch.empty(B * max(K, budget or 0, 1), dtype=i32, device=dev)
         self._active = torch.empty(B * a_max, dtype=i32, device=dev)
-        self._qkv = [torch.empty(B * H * a_max * d, dtype=dtype, device=dev) for _ in range(3)]
+        n_dense = 0 if fused_gather else B * H * a_max * d   # dense Q_A/K_A/V_A copies
+        self._qkv = [torch.empty(n_dense, dtype=dtype, device=dev) for _ in range(3)]
         self._oa = torch.empty(B * H * a_max * d, dtype=dtype, device=dev)
         self.O2 = torch.empty(B, H, N, d, dtype=dtype, device=dev)
         self.O3 = torch.empty(B, H, N, d, dtype=dtype, device=dev)
@@ -113,12 +116,18 @@ class DecodeStep:
         return self.cached_layer(A, layer3, cache, stream=stream)
 
     def cached_layer(self, A: int, layer3, cache, stream=None):
-        """Gather the active rows of layer 3 and run cache-aware attention with the fused
-        cache scatter, using the active set already in ``active(A)``."""
+        """Cache-aware attention of layer 3's active rows with the fused cache scatter, using
+        the active set already in ``active(A)``: in one launch reading the rows in place, or
+        as a gather into dense blocks followed by the attention."""
         Q3, K3, V3 = layer3
         Kc, Vc = cache
         act = self.active(A)
-        qa, ka, va, oa = (self.dense(i, A) for i in range(4))
+        oa = self.dense(3, A)
+        if self.fused_gather:
+            mar_attn_cache_aware_gather(Q3, K3, V3, Kc, Vc, act, O_A=oa, fuse_scatter=True, status=self.status,
+                                        stream=stream)
+            return ("cached", oa, act)
+        qa, ka, va = (self.dense(i, A) for i in range(3))
         mar_kv_gather([Q3, K3, V3], act, dsts=[qa, ka, va], status=self.status, stream=stream)
         mar_attn_cache_aware(qa, ka, va, Kc, Vc, act, O_A=oa, fuse_scatter=True, status=self.status,
                              stream=stream)

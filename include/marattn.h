@@ -213,6 +213,33 @@ int mar_attn_cache_aware(const mar_shape *shape, int32_t A, const void *Q_A,
                          mar_stream_t stream);
 
 /*
+ * mar_attn_cache_aware_gather -- mar_attn_cache_aware with the active gather
+ * folded in: the gather of the active rows, the cache-aware attention and the
+ * cache update of one cached layer in one launch.
+ *
+ * [M] Overall Architecture and Key Design 2: the cached layers compute fresh
+ * Q/K/V only for the active tokens. Here the fresh tensors are whole [B,H,N,d]
+ * tensors and the active rows are read from them in place:
+ *   Q_A[b,h,a,:] = Q[b,h,active_idx[b,a],:]   (K_A, V_A likewise)
+ * and the result is exactly mar_attn_cache_aware(Q_A, K_A, V_A, ...) (the same
+ * kernels, reading the rows through active_idx instead of from dense copies).
+ * With fuse_scatter = 1 the cache rows at the active positions receive the fresh
+ * rows:  K_cache[b,h,p,:] = K[b,h,p,:] for p in active_idx[b] (V likewise).
+ *  Q, K, V             [B,H,N,d] fresh tensors (read only at active positions).
+ *  K_cache, V_cache    [B,H,N,d]; must not be the same buffers as K, V or Q.
+ *  O_A                 [B,H,A,d];  lse_out [B,H,A] fp32 or NULL.
+ *  active_idx          [B,A] distinct positions in [0,N); an out-of-range or
+ *                      repeated position sets MAR_STATUS_INDEX_RANGE / _DUP and
+ *                      leaves the output unspecified (no fault).
+ * A == 0 is a no-op. Limits: N <= 16384 and B*H*N < 2^31 (MAR_ERR_SHAPE).
+ */
+int mar_attn_cache_aware_gather(const mar_shape *shape, int32_t A, const void *Q, const void *K,
+                                const void *V, void *K_cache, void *V_cache,
+                                const int32_t *active_idx, void *O_A, float scale,
+                                float *lse_out, int32_t fuse_scatter, uint32_t *d_status,
+                                mar_stream_t stream);
+
+/*
  * mar_kv_scatter -- write refreshed K/V rows into the per-layer cache.
  *
  * [M] Key Design 2: active tokens carry fresh K/V; the cache keeps every

@@ -34,7 +34,7 @@ def lib():
 
 def test_header_declares_the_entry_points():
     names = _declared_functions()
-    for n in ["mar_attn_full", "mar_attn_cache_aware", "mar_kv_scatter", "mar_kv_gather",
+    for n in ["mar_attn_full", "mar_attn_cache_aware", "mar_attn_cache_aware_gather", "mar_kv_scatter", "mar_kv_gather",
               "mar_refresh_topk", "mar_cfg_residual", "mar_status_read"]:
         assert n in names
 
@@ -154,3 +154,18 @@ def test_attn_full_select_validation(lib):
     assert call(out=None) == -1                     # nowhere to write the selection
     assert call(out=FAKE + 2) == -4                 # misaligned
     assert call(shape=_shape(N=5000)) == -2         # top-K limit
+
+
+def test_cache_aware_gather_validation(lib):
+    def call(shape, A=8, q=FAKE, k=FAKE + 256, v=FAKE + 512, kc=FAKE + 1024, vc=FAKE + 1280, idx=FAKE + 2048,
+             o=FAKE + 4096):
+        return lib.mar_attn_cache_aware_gather(shape, A, q, k, v, kc, vc, idx, o, 0.0, None, 1, None, None)
+    assert call(_shape(), A=0) == 0                 # A == 0 is a no-op
+    assert call(_shape(), A=65) == -1               # A > N
+    assert call(_shape(), idx=None) == -1           # NULL positions
+    assert call(_shape(), kc=FAKE + 256) == -1      # K cache is the fresh K
+    assert call(_shape(), vc=FAKE) == -1            # V cache is the fresh Q
+    assert call(_shape(), o=FAKE + 4104) == -4      # misaligned output
+    assert call(_shape(d=100)) == -2                # unsupported head dim
+    assert call(_shape(N=20000)) == -2              # beyond the cached-list limit
+    assert call(_shape(B=4096, H=64, N=16384)) == -2  # gather rows past 2^31

@@ -33,7 +33,8 @@ def _schedule(cfg):
     return sched, gens
 
 
-def test_decode_loop_mar_l():
+@pytest.mark.parametrize("fused_gather", [True, False])
+def test_decode_loop_mar_l(fused_gather):
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA device")
     cfg = workloads.CONFIGS["mar_l_loop"]
@@ -46,7 +47,8 @@ def test_decode_loop_mar_l():
     Kc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
     Vc = torch.zeros_like(Kc)
     a_max = 2 * max(sched) + cfg.K
-    step = DecodeStep(cfg.Bp, cfg.H, cfg.N, cfg.d, cfg.K, a_max, device=dev, max_gen=max(sched))
+    step = DecodeStep(cfg.Bp, cfg.H, cfg.N, cfg.d, cfg.K, a_max, device=dev, max_gen=max(sched),
+                      fused_gather=fused_gather)
     rows = [0, cfg.B, cfg.Bp - 1]
     orc = OracleRows(rows, cfg.K)
     ties, checked = [], 0

@@ -267,6 +267,117 @@ def test_cache_aware_reports_bad_indices():
     assert mar.mar_status_read(st) & mar.MAR_STATUS_INDEX_RANGE
 
 
+# ------------------------------------------------------------------------------ gather + cache-aware in one call
+GATHER_CASES = [(1, 2, 64, 8, 32), (2, 3, 300, 70, 64), (2, 2, 320, 40, 80), (1, 2, 100, 100, 64),
+                (2, 2, 50, 1, 128), (1, 1, 1088, 114, 80), (3, 2, 257, 130, 64), (2, 3, 320, 3, 64),
+                (1, 2, 640, 301, 80)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("B,H,N,A,d", GATHER_CASES)
+def test_cache_aware_gather_small(dtype, B, H, N, A, d):
+    # the active rows read in place from the fresh tensors: the oracle gathers on the host
+    t = DT[dtype]
+    idx = _active(B, A, N, 90 + A)
+    Q, K, V = (_rand((B, H, N, d), 91 + i, t) for i in range(3))
+    Kc, Vc = _rand((B, H, N, d), 95, t), _rand((B, H, N, d), 96, t)
+    lse = torch.empty(B, H, A, dtype=torch.float32, device=DEV)
+    st = _status()
+    O = mar.mar_attn_cache_aware_gather(Q, K, V, Kc, Vc, idx, lse_out=lse, status=st)
+    assert mar.mar_status_read(st) == 0
+    QA, KA, VA = (_gather_host(x, idx) for x in (Q, K, V))
+    O_ref, L_ref = oracle.cache_aware(QA, KA, VA, Kc, Vc, idx)
+    P.assert_close(O, O_ref, dtype, "O_A (gathered in the launch)")
+    np.testing.assert_allclose(lse.cpu().numpy(), L_ref, atol=1e-5 if dtype == "f32" else 2e-4, rtol=0)
+    # the same kernels over dense copies of the same rows: identical bits
+    d_ = lambda x: x.to(DEV).contiguous()
+    O2 = mar.mar_attn_cache_aware(d_(QA), d_(KA), d_(VA), Kc, Vc, idx)
+    assert torch.equal(O, O2)
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("bf16", 80), ("f32", 64), ("bf16", 32)])
+def test_cache_aware_gather_fused_scatter_is_bit_exact(dtype, d):
+    t = DT[dtype]
+    B, H, N, A = 3, 2, 200, 37
+    idx = _active(B, A, N, 151)
+    Q, K, V = (_rand((B, H, N, d), 152 + i, t) for i in range(3))
+    Kc, Vc = _rand((B, H, N, d), 155, t), _rand((B, H, N, d), 156, t)
+    Kc0, Vc0 = Kc.clone(), Vc.clone()
+    st = _status()
+    O = mar.mar_attn_cache_aware_gather(Q, K, V, Kc, Vc, idx, fuse_scatter=True, status=st)
+    assert mar.mar_status_read(st) == 0
+    QA, KA, VA = (_gather_host(x, idx) for x in (Q, K, V))
+    O_ref, _ = oracle.cache_aware(QA, KA, VA, Kc0, Vc0, idx)   # reads the pre-scatter cache
+    P.assert_close(O, O_ref, dtype, "O_A")
+    assert np.array_equal(oracle._rows_as_bytes(Kc.cpu()), oracle.scatter(KA, idx.cpu(), Kc0.cpu()))
+    assert np.array_equal(oracle._rows_as_bytes(Vc.cpu()), oracle.scatter(VA, idx.cpu(), Vc0.cpu()))
+
+
+def test_cache_aware_gather_mar_b_full_size():
+    cfg = workloads.CONFIGS["mar_b"]
+    ss = workloads.single_step(cfg, device=DEV)
+    idx = _distinct_rows(torch.cat([ss.gen, ss.just, _active(cfg.Bp, cfg.K, cfg.N, 161)], 1), cfg.N, 162)
+    Kc0, Vc0 = ss.Kc.clone(), ss.Vc.clone()
+    st = _status()
+    O = mar.mar_attn_cache_aware_gather(ss.Q3, ss.K3, ss.V3, ss.Kc, ss.Vc, idx, fuse_scatter=True, status=st)
+    assert mar.mar_status_read(st) == 0
+    QA, KA, VA = (_gather_host(x, idx) for x in (ss.Q3, ss.K3, ss.V3))
+    O_ref, _ = oracle.cache_aware(QA, KA, VA, Kc0, Vc0, idx)
+    P.assert_close(O, O_ref, "bf16", "MAR-B O_A (gathered in the launch)")
+    assert np.array_equal(oracle._rows_as_bytes(ss.Kc.cpu()), oracle.scatter(KA, idx.cpu(), Kc0.cpu()))
+
+
+@pytest.mark.parametrize("name,A", [("mar_h", 160), ("mar_h", 6), ("px512", 114)])
+def test_cache_aware_gather_config_sampled_rows(name, A):
+    cfg = workloads.CONFIGS[name]
+    shape = (cfg.Bp, cfg.H, cfg.N, cfg.d)
+    Q, K, V = (_rand(shape, 501 + i, torch.bfloat16) for i in range(3))
+    Kc, Vc = _rand(shape, 505, torch.bfloat16), _rand(shape, 506, torch.bfloat16)
+    idx = _active(cfg.Bp, A, cfg.N, 510 + A)
+    O = mar.mar_attn_cache_aware_gather(Q, K, V, Kc, Vc, idx)
+    torch.cuda.synchronize()
+    for b in (0, cfg.Bp // 2 + 1, cfg.Bp - 1):
+        sl = slice(b, b + 1)
+        QA, KA, VA = (_gather_host(x[sl], idx[sl]) for x in (Q, K, V))
+        O_ref, _ = oracle.cache_aware(QA, KA, VA, Kc[sl], Vc[sl], idx[sl])
+        P.assert_close(O[sl], O_ref, "bf16", f"{name} A={A} row {b}")
+
+
+@pytest.mark.parametrize("d", [64, 80])
+def test_cache_aware_gather_stale_rows_never_contribute(d):
+    B, H, N, A = 3, 4, 320, 40
+    idx = _active(B, A, N, 181 + d)
+    Q, K, V = (_rand((B, H, N, d), 182 + i, torch.bfloat16) for i in range(3))
+    Kc, Vc = _rand((B, H, N, d), 186, torch.bfloat16), _rand((B, H, N, d), 187, torch.bfloat16)
+    Kp, Vp = Kc.clone(), Vc.clone()
+    for b in range(B):
+        Kp[b][:, idx[b].long()] = float("nan")
+        Vp[b][:, idx[b].long()] = float("nan")
+    O = mar.mar_attn_cache_aware_gather(Q, K, V, Kp, Vp, idx)
+    QA, KA, VA = (_gather_host(x, idx) for x in (Q, K, V))
+    O_ref, _ = oracle.cache_aware(QA, KA, VA, Kc, Vc, idx)
+    P.assert_close(O, O_ref, "bf16", "O_A with poisoned stale rows")
+
+
+@pytest.mark.parametrize("dtype,d,N,A", [("bf16", 64, 64, 4), ("f32", 32, 64, 4), ("bf16", 64, 8, 8),
+                                         ("bf16", 80, 64, 4)])
+def test_cache_aware_gather_reports_bad_indices(dtype, d, N, A):
+    t = DT[dtype]
+    B, H = 2, 2
+    Q = _rand((B, H, N, d), 171, t)
+    Kc, Vc = _rand((B, H, N, d), 172, t), _rand((B, H, N, d), 173, t)
+    dup = torch.arange(A, dtype=torch.int32, device=DEV).repeat(B, 1)
+    dup[0, 2] = dup[0, 1]
+    st = _status()
+    mar.mar_attn_cache_aware_gather(Q, Q, Q, Kc, Vc, dup, status=st)
+    assert mar.mar_status_read(st) & mar.MAR_STATUS_INDEX_DUP
+    bad = torch.arange(A, dtype=torch.int32, device=DEV).repeat(B, 1)
+    bad[0, 2], bad[1, 1] = N, -1
+    st = _status()
+    mar.mar_attn_cache_aware_gather(Q, Q, Q, Kc, Vc, bad, fuse_scatter=True, status=st)
+    assert mar.mar_status_read(st) & mar.MAR_STATUS_INDEX_RANGE
+
+
 # ------------------------------------------------------------------------------ gather / scatter
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_gather_and_scatter_bit_exact(dtype):
