@@ -68,6 +68,7 @@ def load(path: str | None = None):
         "mar_last_cuda_error": ([], ctypes.c_int),
         "mar_version": ([], ctypes.c_int),
         "mar_attn_full_workspace_bytes": ([SP, I32, ctypes.c_int], SZ),
+        "mar_attn_full_min_workspace_bytes": ([SP, I32, ctypes.c_int], SZ),
         "mar_attn_full": ([SP, P, P, P, P, F, P, I32, P, P, P, SZ, P, P], ctypes.c_int),
         "mar_attn_full_refresh": ([SP, P, P, P, P, P, P, F, P, P, P], ctypes.c_int),
         "mar_attn_full_select": ([SP, P, P, P, P, F, P, I32, P, I32, I32, P, P, P, P, P, SZ, P, P], ctypes.c_int),

@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/marattn.h: argument validation, workspace
 // accounting and kernel dispatch. Every entry point validates on the host, launches on
 // the caller's stream and returns without synchronising (except mar_status_read).
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -77,9 +78,30 @@ int mar_last_cuda_error(void) { return g_last_cuda; }
 
 int mar_version(void) { return 10000; }
 
+// Score scratch: with the tcgen05 attention (bf16, d = 64 or 80) and G <= 64 the attention
+// launch leaves the generating rows' raw scores (fp32 [B*H, G, N]) for a small reduction;
+// otherwise a separate score kernel keeps per-head fp64 partials ([B*H, N]).
+static constexpr int kMaxFusedG = 32;
+static bool fused_score_shape(const mar_shape *s, int32_t G) {
+    if (s->dtype != MAR_BF16 || G <= 0 || G > kMaxFusedG || (long long)s->H * G * 16 > 40 * 1024 || (s->N & 3))
+        return false;
+    mar::AttnParams p{};
+    p.d = s->d;
+    return mar::attn_tc5_supported(p);
+}
+static size_t ws_rows(const mar_shape *s, int32_t G) {  // raw scores, then (m, l) per row
+    return round_up(sizeof(float) * (size_t)s->B * s->H * G * s->N) + round_up(sizeof(float) * 2 * s->B * s->H * G);
+}
+static size_t ws_partials(const mar_shape *s) { return round_up(sizeof(double) * (size_t)s->B * s->H * s->N); }
+
 size_t mar_attn_full_workspace_bytes(const mar_shape *s, int32_t G, int want_score) {
     if (check_shape(s) != MAR_OK || !want_score || G <= 0) return 0;
-    return round_up(sizeof(double) * (size_t)s->B * s->H * s->N);
+    return fused_score_shape(s, G) ? ws_rows(s, G) : ws_partials(s);
+}
+
+size_t mar_attn_full_min_workspace_bytes(const mar_shape *s, int32_t G, int want_score) {
+    const size_t need = mar_attn_full_workspace_bytes(s, G, want_score);
+    return need ? std::min(need, ws_partials(s)) : 0;
 }
 
 // Full attention, optionally with the layer-2 score and, when `select`, the top-K refresh
@@ -106,10 +128,11 @@ static int attn_full_core(const mar_shape *s, const void *Q, const void *K, cons
         if (!out_idx && !active_out && Ksel > 0) return MAR_ERR_ARG;
         if (!aligned4(out_idx) || !aligned4(active_out)) return MAR_ERR_ALIGN;
     }
-    const size_t need = mar_attn_full_workspace_bytes(s, G, want_score);
-    if (need && (!workspace || workspace_bytes < need ||
-                 (reinterpret_cast<uintptr_t>(workspace) % kWsAlign)))
-        return MAR_ERR_WORKSPACE;
+    // the score's scratch: the raw-row form when it fits (see mar_attn_full_workspace_bytes),
+    // else the per-head partials of the separate score kernel
+    const bool ws_ok = workspace && !(reinterpret_cast<uintptr_t>(workspace) % kWsAlign);
+    const bool fused = want_score && fused_score_shape(s, G) && ws_ok && workspace_bytes >= ws_rows(s, G);
+    if (want_score && !fused && (!ws_ok || workspace_bytes < ws_partials(s))) return MAR_ERR_WORKSPACE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
     mar::AttnParams p{};
@@ -118,10 +141,18 @@ static int attn_full_core(const mar_shape *s, const void *Q, const void *K, cons
     p.B = s->B; p.H = s->H; p.N = s->N; p.d = s->d;
     p.nq = s->N; p.n_dense = s->N; p.A = 0; p.fuse_scatter = 0;
     p.scale = resolve_scale(scale, s->d);
+    if (fused) {
+        p.gen = gen_idx; p.G = G; p.gen_s = static_cast<float *>(workspace);
+        p.gen_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
+                                              round_up(sizeof(float) * (size_t)s->B * s->H * G * s->N));
+    }
     cudaError_t e = (s->dtype == MAR_BF16) ? mar::launch_attn_bf16(p, st) : mar::launch_attn_f32(p, st);
     if (e != cudaSuccess) return cuda_fail(e);
 
-    if (want_score) {
+    if (fused) {
+        e = mar::launch_score_rows(p.gen_s, p.gen_ml, gen_idx, score_out, s->B, s->H, G, s->N, p.scale, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+    } else if (want_score) {
         mar::ScoreParams sp{};
         sp.Q = Q; sp.K = K; sp.gen = gen_idx;
         sp.partial = static_cast<double *>(workspace);
@@ -131,13 +162,13 @@ static int attn_full_core(const mar_shape *s, const void *Q, const void *K, cons
         sp.scale = p.scale;
         e = mar::launch_score(sp, st);
         if (e != cudaSuccess) return cuda_fail(e);
-        if (select && (out_idx || active_out)) {
-            mar::TopkParams tp{};
-            tp.score = score_out; tp.exclude = exclude_idx; tp.out = out_idx; tp.active = active_out;
-            tp.status = d_status; tp.B = s->B; tp.N = s->N; tp.E = E; tp.K = Ksel;
-            e = mar::launch_topk(tp, st);
-            if (e != cudaSuccess) return cuda_fail(e);
-        }
+    }
+    if (want_score && select && (out_idx || active_out)) {
+        mar::TopkParams tp{};
+        tp.score = score_out; tp.exclude = exclude_idx; tp.out = out_idx; tp.active = active_out;
+        tp.status = d_status; tp.B = s->B; tp.N = s->N; tp.E = E; tp.K = Ksel;
+        e = mar::launch_topk(tp, st);
+        if (e != cudaSuccess) return cuda_fail(e);
     }
     return MAR_OK;
 }

@@ -31,6 +31,16 @@ struct AttnParams {
     int nq, n_dense, A;
     int fuse_scatter;
     int fresh;          // cache-aware only: Q/Kd/Vd are [B*H, N, d], active row a at idx[b, a]
+    // Full attention (tcgen05 kernel): the rows of the generating queries gen[b, 0..G) also
+    // leave their raw scores and softmax statistics for the layer-2 score (under the first
+    // slot g of a position listed more than once):
+    //   gen_s[bh, g, j] = q_{gen[b,g]} . k_j (unscaled; the fp32 tensor-core accumulation the
+    //   attention itself uses), gen_ml[bh, g] = (m, l) of the row's own online softmax:
+    //   weight_j = 2^(gen_s * scale * log2(e) - m) / l.
+    const int32_t *gen; // [B, G] or nullptr
+    int G;              // <= 32
+    float *gen_s;       // [B*H, G, N]
+    float2 *gen_ml;     // [B*H, G]
     int store_kv;       // full attention only: Kc/Vc := Kd/Vd (tcgen05 kernel only)
     float scale;        // softmax scale
 };

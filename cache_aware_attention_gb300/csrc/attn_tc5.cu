@@ -117,7 +117,48 @@ MAR_DEVINL uint32_t lane_addr(uint32_t tm, int warp, int col) {
     return tm + ((uint32_t)(32 * warp) << 16) + (uint32_t)col;
 }
 
-template <int D>
+// kGen: full attention that also leaves the generating rows' raw scores (a separate
+// instantiation, so that the other launches keep the code they had without it).
+MAR_DEVINL void st_global_v4_if(bool pred, float *ptr, float a, float b, float c, float d) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %0, 0;\n @p st.global.v4.f32 [%1], {%2, %3, %4, %5};\n}\n" ::"r"(
+            (uint32_t)pred),
+        "l"(ptr), "f"(a), "f"(b), "f"(c), "f"(d));
+}
+// 64 consecutive floats v[0..63] to ptr (16-byte aligned) when pred: one predicate, one base.
+MAR_DEVINL void st_global_row64_if(bool pred, float *ptr, const float *v) {
+#define MAR_ST4(o, i) "@p st.global.v4.f32 [%1+" #o "], {%" #i ", %" #i "+1, %" #i "+2, %" #i "+3};\n"
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %0, 0;\n"
+        "@p st.global.v4.f32 [%1+0], {%2, %3, %4, %5};\n"
+        "@p st.global.v4.f32 [%1+16], {%6, %7, %8, %9};\n"
+        "@p st.global.v4.f32 [%1+32], {%10, %11, %12, %13};\n"
+        "@p st.global.v4.f32 [%1+48], {%14, %15, %16, %17};\n"
+        "@p st.global.v4.f32 [%1+64], {%18, %19, %20, %21};\n"
+        "@p st.global.v4.f32 [%1+80], {%22, %23, %24, %25};\n"
+        "@p st.global.v4.f32 [%1+96], {%26, %27, %28, %29};\n"
+        "@p st.global.v4.f32 [%1+112], {%30, %31, %32, %33};\n"
+        "@p st.global.v4.f32 [%1+128], {%34, %35, %36, %37};\n"
+        "@p st.global.v4.f32 [%1+144], {%38, %39, %40, %41};\n"
+        "@p st.global.v4.f32 [%1+160], {%42, %43, %44, %45};\n"
+        "@p st.global.v4.f32 [%1+176], {%46, %47, %48, %49};\n"
+        "@p st.global.v4.f32 [%1+192], {%50, %51, %52, %53};\n"
+        "@p st.global.v4.f32 [%1+208], {%54, %55, %56, %57};\n"
+        "@p st.global.v4.f32 [%1+224], {%58, %59, %60, %61};\n"
+        "@p st.global.v4.f32 [%1+240], {%62, %63, %64, %65};\n"
+        "}\n" ::"r"((uint32_t)pred),
+        "l"(ptr), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+        "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]),
+        "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]),
+        "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31]), "f"(v[32]), "f"(v[33]), "f"(v[34]),
+        "f"(v[35]), "f"(v[36]), "f"(v[37]), "f"(v[38]), "f"(v[39]), "f"(v[40]), "f"(v[41]), "f"(v[42]), "f"(v[43]),
+        "f"(v[44]), "f"(v[45]), "f"(v[46]), "f"(v[47]), "f"(v[48]), "f"(v[49]), "f"(v[50]), "f"(v[51]), "f"(v[52]),
+        "f"(v[53]), "f"(v[54]), "f"(v[55]), "f"(v[56]), "f"(v[57]), "f"(v[58]), "f"(v[59]), "f"(v[60]), "f"(v[61]),
+        "f"(v[62]), "f"(v[63]));
+#undef MAR_ST4
+}
+
+template <int D, bool kGen>
 __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Params<D> P) {
     using C = Cfg<D>;
     constexpr int S = C::kStages;
@@ -457,7 +498,19 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             __syncwarp();
             return true;
         };
-        if (P.gather && p.fresh) {
+        if (kGen) {
+            // generating positions out of range: reported once per batch row (its first tile
+            // of head 0); such a slot has no row and adds nothing to the score
+            for (int it = 0; it < my_tiles; ++it) {
+                const int tile = (int)blockIdx.x + it * (int)gridDim.x;
+                const int bh = tile / nqt, q0 = (tile % nqt) * BM;
+                if (q0 != 0 || bh % p.H != 0) continue;
+                bool bad = false;
+                for (int gg = lane; gg < p.G; gg += 32)
+                    bad |= (unsigned)__ldg(p.gen + (int64_t)(bh / p.H) * p.G + gg) >= (unsigned)p.N;
+                if (__any_sync(0xffffffffu, bad) && lane == 0) report(p.status, MAR_STATUS_INDEX_RANGE);
+            }
+        } else if (P.gather && p.fresh) {
             bool ok = true;
             uint32_t go_phase = 0;  // bit st: parity of the next DENSE_GO[st] phase
             for (int it = 0; ok && it < my_tiles; ++it) {
@@ -529,12 +582,38 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
         // ------------------------------------------------------------ softmax + epilogue
         const float sl2 = p.scale * kLog2e;
         bool ok = true;
+        int gpos_next = -1;  // full attention with the score: gen[b, lane] of the next tile
+        if constexpr (kGen)
+            if (my_tiles > 0)
+                gpos_next = lane < p.G ? __ldg(p.gen + (int64_t)((int)blockIdx.x / nqt / p.H) * p.G + lane) : -1;
         for (int it = 0; ok && it < my_tiles; ++it) {
             const int tile = (int)blockIdx.x + it * (int)gridDim.x;
             const int bh = tile / nqt, q0 = (tile % nqt) * BM;
             const bool live = (q0 + 32 * warp) < p.nq;  // warp-uniform: some row of this warp is real
             const uint32_t *bm = bitmaps + (it & 1) * bm_words;
             float m_use = 0.f, l = 0.f;
+            // full attention with the layer-2 score: the generating slots g this row serves
+            // full attention with the layer-2 score: the first generating slot this row serves
+            // (a position listed twice is stored once; the reduction reads it for both slots).
+            // Its raw scores go to gen_s row (bh, slot) by predicated stores, so that the other
+            // threads run the same instructions and the block loop keeps one shape.
+            float *gdst = nullptr;
+            uint32_t is_gen = 0, gslot = 0;
+            if constexpr (kGen) {
+                // lane l holds gen[b, l] of this tile's batch row (loaded one tile ahead); the
+                // row's slot is the lowest l whose position is the row
+                const int pos_cur = gpos_next;
+                if (it + 1 < my_tiles) {
+                    const int nb = ((int)blockIdx.x + (it + 1) * (int)gridDim.x) / nqt / p.H;
+                    gpos_next = lane < p.G ? __ldg(p.gen + (int64_t)nb * p.G + lane) : -1;
+                }
+                int slot = -1;
+                for (int gg = p.G - 1; gg >= 0; --gg)
+                    if (__shfl_sync(0xffffffffu, pos_cur, gg) == q0 + tid) slot = gg;
+                is_gen = slot >= 0;
+                gslot = is_gen ? (uint32_t)slot : 0u;
+                gdst = p.gen_s + ((int64_t)bh * p.G + gslot) * p.N;
+            }
             for (int j = 0; j < nblk; ++j) {
                 const int g = it * nblk + j, buf = g % SB;
                 if (j == nd && nc > 0 &&
@@ -576,6 +655,17 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                 if (live) {
                     float v[64];
                     tmem_ld64(lane_addr(tmS0, warp, 64 * buf), v);
+                    if constexpr (kGen) {  // N % 4 == 0: the block's columns in whole float4s
+                        const int ncol = p.N - j * BN;
+                        if (ncol >= 64) {
+                            st_global_row64_if(is_gen, gdst + j * BN, v);
+                        } else {  // the ragged last block (the same branch for every thread)
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                st_global_v4_if(is_gen && 4 * i < ncol, gdst + j * BN + 4 * i, v[4 * i],
+                                                v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                        }
+                    }
                     if (valid != ~0ull) {
 #pragma unroll
                         for (int i = 0; i < 64; ++i) v[i] = ((valid >> i) & 1ull) ? v[i] : -INFINITY;
@@ -684,6 +774,8 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                     }
                 }
                 if (p.lse && row < p.nq) p.lse[(int64_t)bh * p.nq + row] = (m_use + log2f(l)) * kLn2;
+                if constexpr (kGen)
+                    if (is_gen) p.gen_ml[(int64_t)bh * p.G + gslot] = make_float2(m_use, l);
             }
             fence_proxy_async_smem();  // the staged rows, for the TMA store
             __syncwarp();
@@ -721,7 +813,7 @@ int sm_count() {
 template <int D>
 cudaError_t launch(const AttnParams &p, cudaStream_t s) {
     using C = Cfg<D>;
-    static int configured[64] = {0};
+    static int configured[64] = {0}, configured_gen[64] = {0};
     Tc5Params<D> P;
     P.a = p;
     P.gather = p.idx ? 1 : 0;
@@ -753,10 +845,16 @@ cudaError_t launch(const AttnParams &p, cudaStream_t s) {
     P.n_tiles = (int)tiles;
     size_t smem = 1024 + C::oBars + 8 * (KV_FULL + 2 * C::kStages) + 16;
     smem += sizeof(uint32_t) * 2 * 2 * ((p.N + BN - 1) / BN);  // two bitmaps
-    cudaError_t e = ensure_smem(attn_tc5_kernel<D>, smem, configured, /*max_carveout=*/true);
+    const bool gen = p.gen != nullptr && !P.gather;
+    if (gen && (p.G < 1 || p.G > 32)) return cudaErrorInvalidValue;  // one generating slot per lane
+    cudaError_t e = gen ? ensure_smem(attn_tc5_kernel<D, true>, smem, configured_gen, /*max_carveout=*/true)
+                        : ensure_smem(attn_tc5_kernel<D, false>, smem, configured, /*max_carveout=*/true);
     if (e != cudaSuccess) return e;
     const long long grid = tiles < 2LL * sm_count() ? tiles : 2LL * sm_count();
-    attn_tc5_kernel<D><<<(unsigned)grid, kThreads, smem, s>>>(P);
+    if (gen)
+        attn_tc5_kernel<D, true><<<(unsigned)grid, kThreads, smem, s>>>(P);
+    else
+        attn_tc5_kernel<D, false><<<(unsigned)grid, kThreads, smem, s>>>(P);
     return cudaGetLastError();
 }
 

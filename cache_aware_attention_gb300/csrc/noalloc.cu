@@ -60,7 +60,7 @@ int mar_attn_full_noalloc(const mar_shape *s, const void *Q, const void *K, cons
                           float scale, const int32_t *gen_idx, int32_t G, float *score_out, float *lse_out,
                           uint32_t *d_status, mar_stream_t stream) {
     if (!s) return MAR_ERR_ARG;
-    const size_t need = mar_attn_full_workspace_bytes(s, G, score_out != nullptr);
+    const size_t need = mar_attn_full_min_workspace_bytes(s, G, score_out != nullptr);
     if (need > kScratchBytes) return MAR_ERR_SCRATCH_LIMIT;
     void *ws = nullptr;
     if (need) {

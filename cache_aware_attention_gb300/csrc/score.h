@@ -21,6 +21,13 @@ struct ScoreParams {
 size_t score_smem_bytes(int N, int d);
 cudaError_t launch_score(const ScoreParams &p, cudaStream_t s);
 
+// The layer-2 score from what the attention launch left for the generating rows: raw
+// scores gen_s [B*H, G, N] (unscaled q . k) and per row the (m, l) of its online softmax
+// (weight_j = 2^(s_j * scale * log2(e) - m) / l):
+// score[b, j] = (1/(H G)) sum_{h,g} weight_{h,g,j} (generating positions out of range add 0).
+cudaError_t launch_score_rows(const float *gen_s, const float2 *gen_ml, const int32_t *gen, float *score, int B,
+                              int H, int G, int N, float scale, cudaStream_t s);
+
 struct TopkParams {
     const float *score;     // [B, N] (pairs: [2B, N])
     const int32_t *exclude; // [B, E] or nullptr (pairs: [2B, E])

@@ -99,9 +99,13 @@ int mar_version(void);
  * [M] Key Design 1: the weights from the G generating queries to every token,
  * averaged over heads (and over the generating queries):
  *   score[b,j] = 1/(H*G) * sum_h sum_g softmax_j(scale * <Q[b,h,gen[b,g],:], K[b,h,j,:]>)
- * The score is evaluated to about 1e-7 relative (fp32 products, sums carried to
- * fp64-grade accuracy) so that the top-K built on it matches an exact evaluation
- * except on near-ties.
+ * The score is accurate to below 1e-6 relative (fp32 dot products and exponentials,
+ * sums over keys and rows carried to fp64-grade accuracy), so that the top-K built on
+ * it matches an exact evaluation except on near-ties. For bf16 with d = 64 or 80,
+ * G <= 64 and N a multiple of 4 the attention launch itself leaves the raw scores of
+ * the generating rows (its tensor-core dot products) and their softmax statistics for
+ * a small reduction launch; other shapes compute the dot products again in a
+ * separate score launch.
  *
  *  Q, K, V, O  [B,H,N,d] (dtype); O may not alias Q, K or V.
  *  scale       softmax scale; 0 selects 1/sqrt(d).
@@ -110,9 +114,14 @@ int mar_version(void);
  *  lse_out     [B,H,N] fp32 or NULL.
  *  workspace   device scratch of mar_attn_full_workspace_bytes() bytes (256-byte
  *              aligned), or NULL when that size is 0. Contents are overwritten;
- *              calls that overlap on the GPU must not share it.
+ *              calls that overlap on the GPU must not share it. The size is
+ *              4*B*H*G*N + 8*B*H*G bytes (each rounded up to 256) where the attention
+ *              launch leaves the raw scores, else 8*B*H*N. A workspace of at least
+ *              mar_attn_full_min_workspace_bytes() but below the full size is also
+ *              accepted: the score is then computed by the separate score launch.
  */
 size_t mar_attn_full_workspace_bytes(const mar_shape *shape, int32_t G, int want_score);
+size_t mar_attn_full_min_workspace_bytes(const mar_shape *shape, int32_t G, int want_score);
 int mar_attn_full(const mar_shape *shape, const void *Q, const void *K, const void *V,
                   void *O, float scale, const int32_t *gen_idx, int32_t G,
                   float *score_out, float *lse_out, void *workspace,
@@ -166,8 +175,9 @@ int mar_attn_full_refresh(const mar_shape *shape, const void *Q, const void *K, 
  * arguments except the workspace: the score's scratch lives in a buffer compiled into
  * the library (mar_noalloc_scratch_bytes() bytes, 24 MiB, held on every GPU that loads
  * the library until the process exits).
- *  - Returns MAR_ERR_SCRATCH_LIMIT when mar_attn_full_workspace_bytes() of the shape
- *    exceeds that buffer (B*H*N above 3,145,728 with a score requested).
+ *  - Returns MAR_ERR_SCRATCH_LIMIT when mar_attn_full_min_workspace_bytes() of the
+ *    shape exceeds that buffer (B*H*N above 3,145,728 with a score requested, and
+ *    4*B*H*G*N above 24 MiB where the raw-score form applies).
  *  - Allocates nothing. The first call made on a device looks up the buffer's device
  *    address; make that first call before any stream capture.
  *  - All calls share the one buffer: calls that can overlap on the GPU (different

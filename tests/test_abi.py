@@ -71,8 +71,12 @@ def test_attn_full_validation(lib):
     # score without workspace
     assert lib.mar_attn_full(*args(_shape(), score=FAKE, G=4, gen=FAKE)) == -5
     need = lib.mar_attn_full_workspace_bytes(_shape(), 4, 1)
-    assert need >= 2 * 2 * 64 * 8 and need % 256 == 0
-    assert lib.mar_attn_full(*args(_shape(), score=FAKE, G=4, gen=FAKE, ws=FAKE, wb=need - 1)) == -5
+    assert need == 4 * 2 * 2 * 4 * 64 + 256 and need % 256 == 0  # raw-score rows + (m, l) (bf16, d = 64)
+    least = lib.mar_attn_full_min_workspace_bytes(_shape(), 4, 1)
+    assert least == 8 * 2 * 2 * 64                               # per-head partials
+    assert lib.mar_attn_full_workspace_bytes(_shape(d=32), 4, 1) == least   # no raw-score form
+    assert lib.mar_attn_full_workspace_bytes(_shape(), 33, 1) == least      # G above 32
+    assert lib.mar_attn_full(*args(_shape(), score=FAKE, G=4, gen=FAKE, ws=FAKE, wb=least - 1)) == -5
     assert lib.mar_attn_full(*args(_shape(B=0))) == 0             # empty: no-op
 
 

@@ -469,6 +469,48 @@ def test_score_shapes(B, H, N, d, dtype, G):
     assert rel.max() < 1e-6, f"score relative error {rel.max():.3g}"
 
 
+@pytest.mark.parametrize("d,N,G", [(64, 320, 4), (80, 320, 4), (64, 333, 7), (80, 1088, 25), (64, 200, 32),
+                                   (64, 200, 33)])
+def test_score_raw_rows_and_partials_agree(d, N, G):
+    # bf16 with d = 64/80: a workspace of the full size takes the raw-score rows the
+    # attention launch leaves; one of the minimum size takes the separate score launch
+    B, H = 3, 12
+    Q, Kt, V = (_rand((B, H, N, d), 540 + i, torch.bfloat16) for i in range(3))
+    gen = workloads.distinct_positions(B, G, 0, N, 550).to(DEV)
+    ref = oracle.l2_score(Q, Kt, gen)
+    s = mar.MarShape(B, H, N, d, mar.MAR_BF16)
+    full = mar.load().mar_attn_full_workspace_bytes(s, G, 1)
+    least = mar.load().mar_attn_full_min_workspace_bytes(s, G, 1)
+    up = lambda n: n + (-n) % 256
+    assert least == up(8 * B * H * N)
+    raw = N % 4 == 0 and G <= 32          # the raw-row form: N % 4 == 0, at most 32 generating queries
+    assert full == (up(4 * B * H * G * N) + up(8 * B * H * G) if raw else least)
+    errs = []
+    for nbytes in (full, least):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+        score = torch.empty(B, N, dtype=torch.float32, device=DEV)
+        st = _status()
+        mar.mar_attn_full(Q, Kt, V, gen_idx=gen, score_out=score, workspace=ws, status=st)
+        assert mar.mar_status_read(st) == 0
+        rel = np.abs(score.cpu().numpy().astype(np.float64) - ref) / ref
+        errs.append(rel.max())
+    print(f"score relative error: raw rows {errs[0]:.3g}, partials {errs[1]:.3g}")
+    assert max(errs) < 1e-6, errs
+
+
+def test_score_raw_rows_repeated_generating_position():
+    # a position listed twice counts twice in the average, as in the oracle
+    B, H, N, d = 2, 4, 256, 64
+    Q, Kt, V = (_rand((B, H, N, d), 560 + i, torch.bfloat16) for i in range(3))
+    gen = torch.tensor([[5, 77, 5], [200, 3, 3]], dtype=torch.int32, device=DEV)
+    score = torch.empty(B, N, dtype=torch.float32, device=DEV)
+    st = _status()
+    mar.mar_attn_full(Q, Kt, V, gen_idx=gen, score_out=score, status=st)
+    assert mar.mar_status_read(st) == 0
+    ref = oracle.l2_score(Q, Kt, gen)
+    assert (np.abs(score.cpu().numpy().astype(np.float64) - ref) / ref).max() < 1e-6
+
+
 @pytest.mark.parametrize("B,H,N,d,G,E,K", [
     (8, 12, 320, 64, 4, 8, 32),       # MAR-B head shape
     (2, 16, 1088, 80, 6, 12, 64),     # 512 px shape
