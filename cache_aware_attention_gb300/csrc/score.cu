@@ -31,6 +31,7 @@
 #include <cooperative_groups.h>
 
 #include "common.cuh"
+#include "gen_rows.cuh"
 #include "score.h"
 #include "tc5.cuh"
 
@@ -439,22 +440,9 @@ cudaError_t launch_partial_d(const ScoreParams &p, cudaStream_t s) {
     }
 }
 
-// Grid (batch row b, chunk of 128 keys), 512 threads: four groups of 128, one key per
-// thread, each over a quarter of the rows. The attention launch left, per generating row
-// (b, h, g), its raw scores s_j and the (m, l) of its own online softmax, in which the
-// weight of key j is 2^(s_j * scale * log2(e) - m) / l (the same exponential the attention
-// used for l). A group sums its rows' weights in row order (double-float, two interleaved
-// accumulators merged at the end), and the groups' sums are merged in group order. A
-// generating position listed twice was stored once, under its first slot, which both
-// slots read; a position out of [0, N) has no row (the attention launch reports it): it
-// adds 0, and the average stays over H * G.
-constexpr int kRKeys = 128, kRGroups = 4, kRThreads = kRKeys * kRGroups;
-
-struct RowStat {
-    float m, rl;  // max, 1 / l; rl == 0: no row
-    int src;      // row of gen_s holding the slot's scores
-    int pad;
-};
+// Grid (batch row b, chunk of 128 keys), 512 threads: one score group per 128 threads,
+// one key per thread; the groups' sums are merged in group order (see gen_rows.cuh).
+constexpr int kRKeys = 128, kRThreads = kRKeys * kScoreGroups;
 
 __global__ void __launch_bounds__(kRThreads) score_rows_kernel(const float *__restrict__ gen_s,
                                                                const float2 *__restrict__ gen_ml,
@@ -462,52 +450,19 @@ __global__ void __launch_bounds__(kRThreads) score_rows_kernel(const float *__re
                                                                float *__restrict__ score, int H, int G, int N,
                                                                float sl2) {
     extern __shared__ RowStat rstat[];  // [H * G]
-    __shared__ float part[2][kRGroups][kRKeys];
+    __shared__ float part[2][kScoreGroups][kRKeys];
     const int b = blockIdx.x, rows = H * G, tid = threadIdx.x;
-    const int32_t *gb = gen + (int64_t)b * G;
-    for (int r = tid; r < rows; r += kRThreads) {
-        const int g = r % G, pos = gb[g];
-        RowStat st{0.f, 0.f, 0, 0};
-        if ((unsigned)pos < (unsigned)N) {
-            int first = g;
-            for (int q = g - 1; q >= 0; --q)
-                if (gb[q] == pos) first = q;
-            st.src = r - g + first;
-            const float2 ml = gen_ml[(int64_t)b * rows + st.src];
-            st.m = ml.x;
-            st.rl = __frcp_rn(ml.y);
-        }
-        rstat[r] = st;
-    }
+    load_row_stats(rstat, gen_ml, gen, b, H, G, N, tid, kRThreads);
     __syncthreads();
-    const int grp = tid / kRKeys, kk = tid % kRKeys, j = blockIdx.y * kRKeys + kk;
-    const int per = (rows + kRGroups - 1) / kRGroups;
-    const int r_lo = grp * per, r_hi = min(rows, r_lo + per);
-    float h0 = 0.f, l0 = 0.f, h1 = 0.f, l1 = 0.f;
-    if (j < N) {
-        const float *s = gen_s + (int64_t)b * rows * N + j;
-        for (int r0 = r_lo; r0 < r_hi; r0 += 8) {
-            float x[8];
-            RowStat st[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                st[k] = r0 + k < r_hi ? rstat[r0 + k] : RowStat{0.f, 0.f, 0, 0};
-                x[k] = st[k].rl != 0.f ? s[(int64_t)st[k].src * N] : 0.f;
-            }
-#pragma unroll
-            for (int k = 0; k < 8; k += 2) {
-                if (st[k].rl != 0.f) df_add(h0, l0, fast_exp2(fmaf(x[k], sl2, -st[k].m)) * st[k].rl);
-                if (st[k + 1].rl != 0.f) df_add(h1, l1, fast_exp2(fmaf(x[k + 1], sl2, -st[k + 1].m)) * st[k + 1].rl);
-            }
-        }
-    }
-    df_merge(h0, l0, h1, l1);
-    part[0][grp][kk] = h0;
-    part[1][grp][kk] = l0;
+    const int q = tid / kRKeys, kk = tid % kRKeys, j = blockIdx.y * kRKeys + kk;
+    float hi = 0.f, lo = 0.f;
+    if (j < N) score_group_sum<8>(gen_s + (int64_t)b * rows * N + j, rstat, rows, q, N, sl2, hi, lo);
+    part[0][q][kk] = hi;
+    part[1][q][kk] = lo;
     __syncthreads();
-    if (grp == 0 && j < N) {
-        for (int u = 1; u < kRGroups; ++u) df_merge(h0, l0, part[0][u][kk], part[1][u][kk]);
-        score[(int64_t)b * N + j] = __fdiv_rn(h0 + l0, (float)rows);
+    if (q == 0 && j < N) {
+        for (int u = 1; u < kScoreGroups; ++u) df_merge(hi, lo, part[0][u][kk], part[1][u][kk]);
+        score[(int64_t)b * N + j] = __fdiv_rn(hi + lo, (float)rows);
     }
 }
 
