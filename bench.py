@@ -48,9 +48,12 @@ CONFIG = "mar_b"
 N_SETS = 3
 REFRESH_PERIOD = 3
 # DRAM bytes (read + write) of one full-attention launch on this workload, from the ncu
-# capture summarised in profiles/attn_tc5_full_mar_b.md (dram__bytes_read.sum +
+# capture summarised in profiles/attn_tc5_mar_b.md (dram__bytes_read.sum +
 # dram__bytes_write.sum); None once the kernel has changed since that capture.
-FULL_ATTN_DRAM_BYTES = 94.4576e6 + 8.120832e6
+FULL_ATTN_DRAM_BYTES = 94.46656e6 + 7.570432e6
+# the same for one cache-aware launch with the active rows read in place and the fused
+# scatter (A = 40)
+CACHE_AWARE_DRAM_BYTES = 70.47424e6 + 1.344512e6
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -188,6 +191,19 @@ def run_mine(args, ws, rank, local):
     A = cfg.A
     sets = [InputSet(cfg, s, dev) for s in range(N_SETS)]
     step = DecodeStep(cfg.Bp, cfg.H, cfg.N, cfg.d, cfg.K, A, device=dev, max_gen=cfg.G)
+    if args.only:
+        # profiling aid: one layer-2 select call (fills the score and the active set the
+        # other calls read), then --reps calls of the named kind, input sets rotating
+        calls, _ = step_calls(cfg, step, mar)
+        if args.only not in calls:
+            raise SystemExit(f"--only: one of {sorted(calls)}")
+        calls["attn_full_select"](sets[0])
+        for r in range(args.reps):
+            calls[args.only](sets[r % N_SETS])
+        torch.cuda.synchronize()
+        if rank == 0:
+            print(json.dumps({"only": args.only, "reps": args.reps, "status": "ok"}))
+        return
     n_cfg = cfg.B * cfg.n_img * cfg.latent
     stream = torch.cuda.current_stream()
 
@@ -250,12 +266,15 @@ def run_mine(args, ws, rank, local):
             "achieved": fa["gbs"], "peak": hbm, "unit": "GB/s",
             "frac": fa["gbs"] / hbm if fa["gbs"] else None, "traffic": FULL_ATTN_DRAM_BYTES,
             "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch "
-                              "(profiles/attn_tc5_full_mar_b.md)",
+                              "(profiles/attn_tc5_mar_b.md)",
             "peak_source": "MEASURED_PEAKS.json hbm_gbs" if "hbm_gbs" in peaks else "fallback 6800 GB/s"}
     ca = brk["cache_aware_gather"]
     roof_ca = {"bound": "hbm", "kernel": "attn_tc5_kernel<64> (cache-aware attention of the active rows read "
                                          "in place, fused scatter, A=40)",
-               "achieved": ca["gbs"], "peak": hbm, "unit": "GB/s", "frac": ca["gbs"] / hbm if ca["gbs"] else None}
+               "achieved": ca["gbs"], "peak": hbm, "unit": "GB/s", "frac": ca["gbs"] / hbm if ca["gbs"] else None,
+               "traffic": CACHE_AWARE_DRAM_BYTES,
+               "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one launch "
+                                 "(profiles/attn_tc5_mar_b.md)"}
     cpu = cpu_baseline(cfg, budget_s=args.cpu_seconds) if (rank == 0 and ws == 1 and not args.no_cpu) else None
     n_launch = sum(launches_per_step(t) for t in range(W, W + K))
     line = {
@@ -288,14 +307,9 @@ def launches_per_step(t):
     return 3 if t % REFRESH_PERIOD == 0 else 5
 
 
-def breakdown(args, cfg, sets, step, mar, W, K, is_full_refresh, reps: int = 24):
-    """Device time of each C-ABI call of the step.
-
-    Each call kind is captured into one CUDA graph of ``reps`` back-to-back calls (the
-    input sets rotating, so that inputs come from HBM, not L2), replayed after one
-    warm-up replay, and timed with CUDA events on the replaying stream; the per-call
-    time is the graph's time / reps (host launch overhead excluded, the short gaps
-    between kernels of a graph included)."""
+def step_calls(cfg, step, mar):
+    """The C-ABI calls of the step (and of the next rows), by name, each a function of one
+    input set, with the algorithmic bytes of one call."""
     A = cfg.A
     act = step.active(A)
     oa = step.dense(3, A)
@@ -343,6 +357,19 @@ def breakdown(args, cfg, sets, step, mar, W, K, is_full_refresh, reps: int = 24)
             "token_cosine": 2 * cfg.Bp * cfg.H * cfg.N * cfg.d * 2 + cfg.Bp * cfg.N * 4,
             "select_recompute": cfg.Bp * cfg.N * 4 * 2 + cfg.Bp * (cfg.G + cfg.J) * 4,
             "topk_pairs": cfg.Bp * cfg.N * 4 + cfg.Bp * (cfg.G + cfg.J + cfg.K) * 4}
+    return calls, algo
+
+
+def breakdown(args, cfg, sets, step, mar, W, K, is_full_refresh, reps: int = 24):
+    """Device time of each C-ABI call of the step.
+
+    Each call kind is captured into one CUDA graph of ``reps`` back-to-back calls (the
+    input sets rotating, so that inputs come from HBM, not L2), replayed after one
+    warm-up replay, and timed with CUDA events on the replaying stream; the per-call
+    time is the graph's time / reps (host launch overhead excluded, the short gaps
+    between kernels of a graph included)."""
+    A = cfg.A
+    calls, algo = step_calls(cfg, step, mar)
     side = torch.cuda.Stream()
     out = {}
     for name, fn in calls.items():
@@ -531,6 +558,10 @@ def main():
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--only", default=None,
+                    help="profiling aid: run REPS calls of one C-ABI call kind of the step "
+                         "(e.g. attn_full, cache_aware_gather) after one layer-2 select call; no timing")
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
