@@ -195,6 +195,7 @@ def run_mine(args, ws, rank, local):
         # profiling aid: one layer-2 select call (fills the score and the active set the
         # other calls read), then --reps calls of the named kind, input sets rotating
         calls, _ = step_calls(cfg, step, mar)
+        calls = {k: v for k, v in calls.items() if not k.startswith(("_", "torch_"))}
         if args.only not in calls:
             raise SystemExit(f"--only: one of {sorted(calls)}")
         calls["attn_full_select"](sets[0])
@@ -319,6 +320,8 @@ def step_calls(cfg, step, mar):
     cos_buf = torch.empty(cfg.Bp, cfg.N, dtype=torch.float32, device=dev)
     sel_idx = torch.empty(cfg.Bp, cfg.N, dtype=torch.int32, device=dev)
     sel_cnt = torch.empty(cfg.Bp, dtype=torch.int32, device=dev)
+    # the cached positions of each row (the complement of the active set), for the context call
+    cached_idx = torch.empty(cfg.Bp, cfg.N - A, dtype=torch.int64, device=dev)
     calls = {
         "attn_full": lambda s: mar.mar_attn_full(s.layer2[0], s.layer2[1], s.layer2[2], step.O2),
         "attn_full+score": lambda s: mar.mar_attn_full(s.layer2[0], s.layer2[1], s.layer2[2], step.O2,
@@ -344,6 +347,10 @@ def step_calls(cfg, step, mar):
                                                                out_count=sel_cnt),
         "topk_pairs": lambda s: mar.mar_refresh_topk_pairs(step.score, s.exclude, cfg.K, out_idx=step.R,
                                                            active_out=act),
+        # context only (not this library): the concatenating alternative of [MARché] Figure 7 --
+        # gather the active rows and the cached rows, concatenate, PyTorch's fused attention,
+        # then the cache update
+        "torch_concat_sdpa (context)": lambda s: torch_concat_sdpa(s, act, cached_idx),
     }
     algo = {"attn_full": bytes_full_attention(cfg),
             "attn_full+score": bytes_full_attention(cfg),
@@ -356,8 +363,27 @@ def step_calls(cfg, step, mar):
             "cfg": 3 * cfg.B * cfg.n_img * cfg.latent * 4,
             "token_cosine": 2 * cfg.Bp * cfg.H * cfg.N * cfg.d * 2 + cfg.Bp * cfg.N * 4,
             "select_recompute": cfg.Bp * cfg.N * 4 * 2 + cfg.Bp * (cfg.G + cfg.J) * 4,
-            "topk_pairs": cfg.Bp * cfg.N * 4 + cfg.Bp * (cfg.G + cfg.J + cfg.K) * 4}
+            "topk_pairs": cfg.Bp * cfg.N * 4 + cfg.Bp * (cfg.G + cfg.J + cfg.K) * 4,
+            "torch_concat_sdpa (context)": bytes_cache_aware(cfg, A) + 2 * cfg.Bp * cfg.H * A * cfg.d * 2}
+    calls["_cached_idx"] = cached_idx
     return calls, algo
+
+
+def torch_concat_sdpa(s, act, cached_idx):
+    """Cache-aware attention the concatenating way, with PyTorch ops (context only)."""
+    import torch.nn.functional as F
+    Q3, K3, V3 = s.layer3
+    Kc, Vc = s.cache
+    B, H, N, d = Q3.shape
+    ia = act.long()[:, None, :, None].expand(-1, H, -1, d)
+    ic = cached_idx[:, None, :, None].expand(-1, H, -1, d)
+    qa, ka, va = (torch.gather(x, 2, ia) for x in (Q3, K3, V3))
+    k = torch.cat([ka, torch.gather(Kc, 2, ic)], 2)
+    v = torch.cat([va, torch.gather(Vc, 2, ic)], 2)
+    o = F.scaled_dot_product_attention(qa, k, v)
+    Kc.scatter_(2, ia, ka)
+    Vc.scatter_(2, ia, va)
+    return o
 
 
 def breakdown(args, cfg, sets, step, mar, W, K, is_full_refresh, reps: int = 24):
@@ -370,9 +396,19 @@ def breakdown(args, cfg, sets, step, mar, W, K, is_full_refresh, reps: int = 24)
     between kernels of a graph included)."""
     A = cfg.A
     calls, algo = step_calls(cfg, step, mar)
+    cached_idx = calls.pop("_cached_idx")
+
+    def set_cached_idx():  # the complement of the current active set, per row (outside the timing)
+        torch.cuda.synchronize()
+        mask = torch.ones(cfg.Bp, cfg.N, dtype=torch.bool, device=cached_idx.device)
+        mask.scatter_(1, step.active(A).long(), False)
+        cached_idx.copy_(torch.nonzero(mask)[:, 1].view(cfg.Bp, cfg.N - A))
+        torch.cuda.synchronize()
     side = torch.cuda.Stream()
     out = {}
     for name, fn in calls.items():
+        if name.startswith("torch_concat_sdpa"):
+            set_cached_idx()
         fn(sets[0])
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
