@@ -749,28 +749,32 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                 const int row = q0 + tid, r = tid;
                 const float inv = 1.f / l;
                 unsigned char *stage = sm + C::oQ + (it & 1) * C::kQBytes;
+                {  // the 64-column part: one tensor-memory load, eight 16-byte chunks
+                    float o[64];
+                    tmem_ld64(lane_addr(tmO, warp, 0), o);
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 16) {
+                    for (int c = 0; c < 8; ++c) {
+                        uint4 u;
+                        u.x = pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv);
+                        u.y = pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
+                        u.z = pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
+                        u.w = pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+                        *reinterpret_cast<uint4 *>(stage + r * 128 + ((c ^ (r & 7)) << 4)) = u;
+                    }
+                }
+                if constexpr (C::DB > 0) {  // the 16 tail columns
                     float o[16];
-                    tmem_ld16(lane_addr(tmO, warp, c0), o);
-                    uint4 u0, u1;
-                    u0.x = pack_bf16x2(o[0] * inv, o[1] * inv);
-                    u0.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-                    u0.z = pack_bf16x2(o[4] * inv, o[5] * inv);
-                    u0.w = pack_bf16x2(o[6] * inv, o[7] * inv);
-                    u1.x = pack_bf16x2(o[8] * inv, o[9] * inv);
-                    u1.y = pack_bf16x2(o[10] * inv, o[11] * inv);
-                    u1.z = pack_bf16x2(o[12] * inv, o[13] * inv);
-                    u1.w = pack_bf16x2(o[14] * inv, o[15] * inv);
-                    if (c0 < 64) {
-                        const int c = c0 >> 3;  // chunks c, c + 1 of the row
-                        *reinterpret_cast<uint4 *>(stage + r * 128 + ((c ^ (r & 7)) << 4)) = u0;
-                        *reinterpret_cast<uint4 *>(stage + r * 128 + (((c + 1) ^ (r & 7)) << 4)) = u1;
-                    } else {
-                        unsigned char *tail = stage + C::kQa;
-                        const int sw = (r >> 2) & 1;
-                        *reinterpret_cast<uint4 *>(tail + r * 32 + ((0 ^ sw) << 4)) = u0;
-                        *reinterpret_cast<uint4 *>(tail + r * 32 + ((1 ^ sw) << 4)) = u1;
+                    tmem_ld16(lane_addr(tmO, warp, 64), o);
+                    unsigned char *tail = stage + C::kQa;
+                    const int sw = (r >> 2) & 1;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint4 u;
+                        u.x = pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv);
+                        u.y = pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
+                        u.z = pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
+                        u.w = pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+                        *reinterpret_cast<uint4 *>(tail + r * 32 + ((c ^ sw) << 4)) = u;
                     }
                 }
                 if (p.lse && row < p.nq) p.lse[(int64_t)bh * p.nq + row] = (m_use + log2f(l)) * kLn2;
