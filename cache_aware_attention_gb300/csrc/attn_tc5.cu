@@ -566,14 +566,33 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                     const bf16 *Vd = static_cast<const bf16 *>(p.Vd);
                     bf16 *Kc = static_cast<bf16 *>(p.Kc);
                     bf16 *Vc = static_cast<bf16 *>(p.Vc);
-                    for (int t = lane; t < p.A * (D / 8); t += 32) {
-                        const int a = t / (D / 8), c = t % (D / 8);
-                        const int pos = p.idx[(int64_t)b * p.A + a];
-                        if (pos < 0 || pos >= p.N) continue;
-                        const int64_t src = ((int64_t)bh * p.A + a) * D + 8 * c;
-                        const int64_t dst = ((int64_t)bh * p.N + pos) * D + 8 * c;
-                        *reinterpret_cast<uint4 *>(Kc + dst) = *reinterpret_cast<const uint4 *>(Kd + src);
-                        *reinterpret_cast<uint4 *>(Vc + dst) = *reinterpret_cast<const uint4 *>(Vd + src);
+                    // eight 16-byte chunks per lane and pass, all loads before the stores, so
+                    // that the passes are not serialised on the load latency
+                    constexpr int kU = 8;
+                    for (int t0 = 0; t0 < p.A * (D / 8); t0 += 32 * kU) {
+                        uint4 kv[kU], vv[kU];
+                        int64_t dst[kU];
+#pragma unroll
+                        for (int u = 0; u < kU; ++u) {
+                            const int t = t0 + 32 * u + lane;
+                            dst[u] = -1;
+                            if (t < p.A * (D / 8)) {
+                                const int a = t / (D / 8), c = t % (D / 8);
+                                const int pos = __ldg(p.idx + (int64_t)b * p.A + a);
+                                if (pos >= 0 && pos < p.N) {
+                                    const int64_t src = ((int64_t)bh * p.A + a) * D + 8 * c;
+                                    kv[u] = __ldg(reinterpret_cast<const uint4 *>(Kd + src));
+                                    vv[u] = __ldg(reinterpret_cast<const uint4 *>(Vd + src));
+                                    dst[u] = ((int64_t)bh * p.N + pos) * D + 8 * c;
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int u = 0; u < kU; ++u)
+                            if (dst[u] >= 0) {
+                                *reinterpret_cast<uint4 *>(Kc + dst[u]) = kv[u];
+                                *reinterpret_cast<uint4 *>(Vc + dst[u]) = vv[u];
+                            }
                     }
                 }
             }
