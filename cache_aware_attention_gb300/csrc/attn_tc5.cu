@@ -333,6 +333,30 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             if (j == 0 && !mbar_wait(&bars[Q_FULL + (it & 1)], (it >> 1) & 1, p.status, abort_flag)) break;
             if (g >= SB && !mbar_wait(&bars[O_DONE + g % SB], (g / SB - 1) & 1, p.status, abort_flag)) break;
             tc_fence_after();
+            if (j >= nd) {
+                // A cache block: its rows at active positions are stale. Their P will be 0, but
+                // 0 x NaN is NaN, so their V rows are cleared in shared memory here, before S
+                // is issued (PV_g, which reads them, follows S_g through the softmax warps'
+                // hand-over). Whole rows are cleared, so the swizzle inside a row does not matter.
+                if (j == nd && !mbar_wait(&bars[BM_FULL + (it & 1)], (it >> 1) & 1, p.status, abort_flag)) break;
+                const uint32_t *bm = bitmaps + (it & 1) * bm_words;
+                const int pos0 = (j - nd) * BN;
+                uint64_t stale = (uint64_t)bm[pos0 >> 5] | ((uint64_t)bm[(pos0 >> 5) + 1] << 32);
+                if (p.N - pos0 < 64) stale &= (1ull << (p.N - pos0)) - 1ull;
+                if (stale) {
+                    unsigned char *stw = sm + C::oStage + (g % S) * C::kStageBytes;
+                    for (int t = lane; t < BN * 8; t += 32)
+                        if ((stale >> (t >> 3)) & 1ull)
+                            *reinterpret_cast<uint4 *>(stw + C::sVa + 16 * t) = make_uint4(0, 0, 0, 0);
+                    if constexpr (C::DB > 0) {
+                        for (int t = lane; t < BN * 2; t += 32)
+                            if ((stale >> (t >> 1)) & 1ull)
+                                *reinterpret_cast<uint4 *>(stw + C::sVb + 16 * t) = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
+            }
             const unsigned char *sq = sm + C::oQ + (it & 1) * C::kQBytes;
             const unsigned char *stg = sm + C::oStage + (g % S) * C::kStageBytes;
             const uint64_t dQa = smem_desc(sq, 16, 1024, Swz::B128);
@@ -641,35 +665,17 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                 if (!(ok = mbar_wait(&bars[S_FULL + buf], (g / SB) & 1, p.status, abort_flag))) break;
                 tc_fence_after();
                 // slots of this block that are keys: dense rows below n_dense; cache rows below
-                // N whose position is not active (active positions hold stale cache rows)
-                uint64_t valid, stale = 0ull;
+                // N whose position is not active (active positions hold stale cache rows, whose
+                // V rows the S issuer has cleared)
+                uint64_t valid;
                 if (j < nd) {
                     const int r = p.n_dense - j * BN;
                     valid = r >= 64 ? ~0ull : ((1ull << r) - 1ull);
                 } else {
                     const int pos0 = (j - nd) * BN;
-                    stale = (uint64_t)bm[pos0 >> 5] | ((uint64_t)bm[(pos0 >> 5) + 1] << 32);
-                    valid = ~stale;
+                    valid = ~((uint64_t)bm[pos0 >> 5] | ((uint64_t)bm[(pos0 >> 5) + 1] << 32));
                     const int r = p.N - pos0;
-                    if (r < 64) {
-                        valid &= (1ull << r) - 1ull;
-                        stale &= (1ull << r) - 1ull;
-                    }
-                }
-                if (stale) {
-                    // Their P is 0, but 0 x NaN is NaN: clear the stale V rows in shared memory
-                    // so that whatever a stale row holds cannot reach O. Whole rows are cleared,
-                    // so the swizzle inside a row does not matter.
-                    unsigned char *stg = sm + C::oStage + (g % S) * C::kStageBytes;
-                    for (int t = tid; t < BN * 8; t += 128)
-                        if ((stale >> (t >> 3)) & 1ull)
-                            *reinterpret_cast<uint4 *>(stg + C::sVa + 16 * t) = make_uint4(0, 0, 0, 0);
-                    if constexpr (C::DB > 0) {
-                        for (int t = tid; t < BN * 2; t += 128)
-                            if ((stale >> (t >> 1)) & 1ull)
-                                *reinterpret_cast<uint4 *>(stg + C::sVb + 16 * t) = make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();
+                    if (r < 64) valid &= (1ull << r) - 1ull;
                 }
                 if (live) {
                     float v[64];
