@@ -1,5 +1,5 @@
 // Blackwell (sm_100/sm_103) building blocks: mbarriers with bounded waits, TMA tensor
-// loads (tile and gather4), tcgen05 tensor-memory allocation, UMMA shared-memory and
+// tile loads, tcgen05 tensor-memory allocation, UMMA shared-memory and
 // instruction descriptors, tcgen05.mma / commit, and tensor-memory loads/stores.
 //
 // Every wait is bounded: after kSpinLimit polls the waiter records MAR_STATUS_TIMEOUT in
@@ -76,16 +76,6 @@ MAR_DEVINL void tma_load_3d(void *dst, const CUtensorMap *m, int c0, int c1, int
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
         "[%5];\n" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
-        : "memory");
-}
-// Four rows r0..r3 (box width columns starting at column c0) of a 2-D tensor map whose
-// box is one row high; they land as four consecutive box rows at dst.
-MAR_DEVINL void tma_gather4(void *dst, const CUtensorMap *m, int c0, int r0, int r1, int r2, int r3,
-                            uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], "
-        "[%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
         : "memory");
 }
 
