@@ -50,10 +50,10 @@ REFRESH_PERIOD = 3
 # DRAM bytes (read + write) of one full-attention launch on this workload, from the ncu
 # capture summarised in profiles/attn_tc5_mar_b.md (dram__bytes_read.sum +
 # dram__bytes_write.sum); None once the kernel has changed since that capture.
-FULL_ATTN_DRAM_BYTES = 94.46656e6 + 7.570432e6
+FULL_ATTN_DRAM_BYTES = 94.472192e6 + 7.936e6
 # the same for one cache-aware launch with the active rows read in place and the fused
 # scatter (A = 40)
-CACHE_AWARE_DRAM_BYTES = 70.47424e6 + 1.344512e6
+CACHE_AWARE_DRAM_BYTES = 70.90688e6 + 1.603584e6
 
 
 # ----------------------------------------------------------------------------- distributed
