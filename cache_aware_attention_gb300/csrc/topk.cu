@@ -18,7 +18,7 @@
 namespace mar {
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 512;
 constexpr int kMaxN = 4096;
 constexpr int kRankN = 1152;
 
