@@ -11,9 +11,12 @@
 // loads: first the fresh active rows (cache-aware) or all rows (full attention), then,
 // for cache-aware attention, the cache slab of the (b, h) in position order. Cache rows
 // of active positions hold stale values: a bitmap of the active positions masks them out
-// of the softmax and their V rows are cleared in shared memory, so they never contribute
-// (they are read, costing A/N extra bytes, because one tile load per 64 rows runs at the
-// TMA unit's full rate while a per-row gather is bound by its request rate).
+// of the softmax and the S issuer clears their V rows in shared memory, so they never
+// contribute (they are read, costing A/N extra bytes, because one tile load per 64 rows
+// runs at the TMA unit's full rate while a per-row gather is bound by its request rate).
+// The fresh active rows come either as dense [BH, A, d] blocks (TMA tile loads) or are read
+// in place from the whole fresh tensors through the active index (the index warp copies
+// them, 16 bytes per lane, into the same swizzled layouts).
 //
 // Persistent CTAs (two per SM; 8 warps x at most 128 registers, so that the two CTAs'
 // 16 warps fill the four 16K-register sub-partitions of an SM): CTA c processes the
@@ -22,9 +25,11 @@
 //   warp 4     TMA producer: Q of each tile (double-buffered) and the K/V blocks of all
 //              tiles through one ring of stages, running ahead across tile boundaries;
 //              for full attention with the cache refresh it also stores the K/V blocks of
-//              each (b, h)'s first query tile to the cache (TMA tile stores from the stages)
+//              each (b, h)'s first query tile to the cache (TMA tile stores from the stages);
+//              it stores each tile's O, which the epilogue stages in the tile's Q buffer
 //   warp 5     S issuer (one elected lane):  S_g = Q K_g^T  (M=128, N=64, K=d, K-major
-//              operands), once K_g has landed and PV_{g-SB} has released S/P buffer g % SB
+//              operands), once K_g has landed and PV_{g-SB} has released S/P buffer g % SB;
+//              before a cache block's S, the whole warp clears its stale V rows
 //   warp 7     PV issuer (one elected lane): O += P_g V_g  (M=128, N=d, K=64, P from
 //              TMEM, V MN-major), as soon as P_g is written; it releases the K/V stage
 //   warp 6     index warp: bitmap of the active positions of each tile (double-
@@ -39,7 +44,8 @@
 // d = 80), each overwritten in place by P as packed bf16 pairs, and O (d columns)
 // accumulated across the blocks of a tile. With three buffers S_{g+1} depends only on
 // PV_{g-2}, long complete, so the softmax warps run from block to block without waiting
-// for the tensor pipe.
+// for the tensor pipe. The kGen instantiation (full attention with the layer-2 score)
+// also stores the raw scores and (m, l) of the rows that are generating queries.
 // Online softmax with a lazy rescale: a row keeps the max m used for its P values; a
 // block whose row max exceeds m by more than 8 (base-2 units) raises m and rescales O
 // and l by 2^(m_old - m_new); otherwise P = 2^(s - m) <= 2^8 and nothing is rescaled.
