@@ -27,6 +27,7 @@
 //              for full attention with the cache refresh it also stores the K/V blocks of
 //              each (b, h)'s first query tile to the cache (TMA tile stores from the stages);
 //              it stores each tile's O, which the epilogue stages in the tile's Q buffer
+//              (in the gather form the index warp owns the Q buffers and does both)
 //   warp 5     S issuer (one elected lane):  S_g = Q K_g^T  (M=128, N=64, K=d, K-major
 //              operands), once K_g has landed and PV_{g-SB} has released S/P buffer g % SB;
 //              before a cache block's S, the whole warp clears its stale V rows
