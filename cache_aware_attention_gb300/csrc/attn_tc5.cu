@@ -165,7 +165,33 @@ MAR_DEVINL void st_global_row64_if(bool pred, float *ptr, const float *v) {
 #undef MAR_ST4
 }
 
-template <int D, bool kGen>
+// 64 consecutive floats v[0..63] to ptr (32-byte aligned) when pred: eight 256-bit stores.
+MAR_DEVINL void st_global_row64_v8_if(bool pred, float *ptr, const float *v) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %0, 0;\n"
+        "@p st.global.v8.f32 [%1+0], {%2, %3, %4, %5, %6, %7, %8, %9};\n"
+        "@p st.global.v8.f32 [%1+32], {%10, %11, %12, %13, %14, %15, %16, %17};\n"
+        "@p st.global.v8.f32 [%1+64], {%18, %19, %20, %21, %22, %23, %24, %25};\n"
+        "@p st.global.v8.f32 [%1+96], {%26, %27, %28, %29, %30, %31, %32, %33};\n"
+        "@p st.global.v8.f32 [%1+128], {%34, %35, %36, %37, %38, %39, %40, %41};\n"
+        "@p st.global.v8.f32 [%1+160], {%42, %43, %44, %45, %46, %47, %48, %49};\n"
+        "@p st.global.v8.f32 [%1+192], {%50, %51, %52, %53, %54, %55, %56, %57};\n"
+        "@p st.global.v8.f32 [%1+224], {%58, %59, %60, %61, %62, %63, %64, %65};\n"
+        "}\n" ::"r"((uint32_t)pred),
+        "l"(ptr), "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+        "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]),
+        "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]),
+        "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31]), "f"(v[32]), "f"(v[33]), "f"(v[34]),
+        "f"(v[35]), "f"(v[36]), "f"(v[37]), "f"(v[38]), "f"(v[39]), "f"(v[40]), "f"(v[41]), "f"(v[42]), "f"(v[43]),
+        "f"(v[44]), "f"(v[45]), "f"(v[46]), "f"(v[47]), "f"(v[48]), "f"(v[49]), "f"(v[50]), "f"(v[51]), "f"(v[52]),
+        "f"(v[53]), "f"(v[54]), "f"(v[55]), "f"(v[56]), "f"(v[57]), "f"(v[58]), "f"(v[59]), "f"(v[60]), "f"(v[61]),
+        "f"(v[62]), "f"(v[63]));
+}
+
+// kGen: 0 = plain attention; 1 = with the generating rows' raw scores, 16-byte stores;
+// 2 = the same with 32-byte stores (N % 8 == 0 and a 32-byte-aligned score buffer, so that
+// every row and block starts on a 32-byte boundary).
+template <int D, int kGen>
 __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Params<D> P) {
     using C = Cfg<D>;
     constexpr int S = C::kStages;
@@ -690,7 +716,10 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                     if constexpr (kGen) {  // N % 4 == 0: the block's columns in whole float4s
                         const int ncol = p.N - j * BN;
                         if (ncol >= 64) {
-                            st_global_row64_if(is_gen, gdst + j * BN, v);
+                            if constexpr (kGen == 2)
+                                st_global_row64_v8_if(is_gen, gdst + j * BN, v);
+                            else
+                                st_global_row64_if(is_gen, gdst + j * BN, v);
                         } else {  // the ragged last block (the same branch for every thread)
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
@@ -849,7 +878,7 @@ int sm_count() {
 template <int D>
 cudaError_t launch(const AttnParams &p, cudaStream_t s) {
     using C = Cfg<D>;
-    static int configured[64] = {0}, configured_gen[64] = {0};
+    static int configured[64] = {0}, configured_gen[64] = {0}, configured_gen8[64] = {0};
     Tc5Params<D> P;
     P.a = p;
     P.gather = p.idx ? 1 : 0;
@@ -883,14 +912,20 @@ cudaError_t launch(const AttnParams &p, cudaStream_t s) {
     smem += sizeof(uint32_t) * 2 * 2 * ((p.N + BN - 1) / BN);  // two bitmaps
     const bool gen = p.gen != nullptr && !P.gather;
     if (gen && (p.G < 1 || p.G > 32)) return cudaErrorInvalidValue;  // one generating slot per lane
-    cudaError_t e = gen ? ensure_smem(attn_tc5_kernel<D, true>, smem, configured_gen, /*max_carveout=*/true)
-                        : ensure_smem(attn_tc5_kernel<D, false>, smem, configured, /*max_carveout=*/true);
+    // 32-byte raw-score stores when every row and block of the score buffer starts on a
+    // 32-byte boundary (row starts are multiples of 4 N bytes, block starts of 256 bytes)
+    const bool gen8 = gen && (p.N % 8) == 0 && (reinterpret_cast<uintptr_t>(p.gen_s) % 32) == 0;
+    cudaError_t e = gen8  ? ensure_smem(attn_tc5_kernel<D, 2>, smem, configured_gen8, /*max_carveout=*/true)
+                    : gen ? ensure_smem(attn_tc5_kernel<D, 1>, smem, configured_gen, /*max_carveout=*/true)
+                          : ensure_smem(attn_tc5_kernel<D, 0>, smem, configured, /*max_carveout=*/true);
     if (e != cudaSuccess) return e;
     const long long grid = tiles < 2LL * sm_count() ? tiles : 2LL * sm_count();
-    if (gen)
-        attn_tc5_kernel<D, true><<<(unsigned)grid, kThreads, smem, s>>>(P);
+    if (gen8)
+        attn_tc5_kernel<D, 2><<<(unsigned)grid, kThreads, smem, s>>>(P);
+    else if (gen)
+        attn_tc5_kernel<D, 1><<<(unsigned)grid, kThreads, smem, s>>>(P);
     else
-        attn_tc5_kernel<D, false><<<(unsigned)grid, kThreads, smem, s>>>(P);
+        attn_tc5_kernel<D, 0><<<(unsigned)grid, kThreads, smem, s>>>(P);
     return cudaGetLastError();
 }
 

@@ -472,8 +472,9 @@ def test_score_shapes(B, H, N, d, dtype, G):
     assert rel.max() < 1e-6, f"score relative error {rel.max():.3g}"
 
 
+# N % 8 == 0 takes 32-byte raw-score stores, N % 8 == 4 16-byte ones, N % 4 != 0 the separate kernel
 @pytest.mark.parametrize("d,N,G", [(64, 320, 4), (80, 320, 4), (64, 333, 7), (80, 1088, 25), (64, 200, 32),
-                                   (64, 200, 33)])
+                                   (64, 200, 33), (64, 300, 4), (80, 212, 6)])
 def test_score_raw_rows_and_partials_agree(d, N, G):
     # bf16 with d = 64/80: a workspace of the full size takes the raw-score rows the
     # attention launch leaves; one of the minimum size takes the separate score launch
