@@ -111,17 +111,6 @@ MAR_DEVINL void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
-MAR_DEVINL void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "{\n tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
-        " tcgen05.wait::ld.sync.aligned;\n}\n"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
 MAR_DEVINL void tmem_ld64(uint32_t taddr, float (&v)[64]) {
     uint32_t r[64];
     asm volatile(
@@ -133,7 +122,6 @@ MAR_DEVINL void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 #pragma unroll
     for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
-MAR_DEVINL void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 
 MAR_DEVINL void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
@@ -227,10 +215,6 @@ MAR_DEVINL void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;\
 template <int N> MAR_DEVINL void bulk_wait_group_read() {
     asm volatile("cp.async.bulk.wait_group.read %0;\n" ::"n"(N) : "memory");
 }
-// Waits until at most N committed bulk groups of this thread are incomplete.
-template <int N> MAR_DEVINL void bulk_wait_group() {
-    asm volatile("cp.async.bulk.wait_group %0;\n" ::"n"(N) : "memory");
-}
 // Contiguous global -> shared copy by the TMA unit, completing `bytes` on `bar`. Both
 // addresses 16-byte aligned, bytes a multiple of 16.
 MAR_DEVINL void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
@@ -238,18 +222,6 @@ MAR_DEVINL void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
             smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-}  // namespace tc5
-}  // namespace mar
-
-namespace mar {
-namespace tc5 {
-MAR_DEVINL void tma_load_2d(void *dst, const CUtensorMap *m, int c0, int c1, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];\n" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
         : "memory");
 }
 }  // namespace tc5
