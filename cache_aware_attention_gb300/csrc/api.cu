@@ -78,7 +78,7 @@ int mar_last_cuda_error(void) { return g_last_cuda; }
 
 int mar_version(void) { return 10000; }
 
-// Score scratch: with the tcgen05 attention (bf16, d = 64 or 80) and G <= 64 the attention
+// Score scratch: with the tcgen05 attention (bf16, d = 64 or 80), G <= 32 and N % 4 == 0 the attention
 // launch leaves the generating rows' raw scores (fp32 [B*H, G, N]) for a small reduction;
 // otherwise a separate score kernel keeps per-head fp64 partials ([B*H, N]).
 static constexpr int kMaxFusedG = 32;
