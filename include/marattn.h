@@ -102,7 +102,7 @@ int mar_version(void);
  * The score is accurate to below 1e-6 relative (fp32 dot products and exponentials,
  * sums over keys and rows carried to fp64-grade accuracy), so that the top-K built on
  * it matches an exact evaluation except on near-ties. For bf16 with d = 64 or 80,
- * G <= 64 and N a multiple of 4 the attention launch itself leaves the raw scores of
+ * G <= 32 and N a multiple of 4 the attention launch itself leaves the raw scores of
  * the generating rows (its tensor-core dot products) and their softmax statistics for
  * a small reduction launch; other shapes compute the dot products again in a
  * separate score launch.
