@@ -22,14 +22,14 @@ __all__ = [
     "mar_attn_full_noalloc", "mar_attn_full_refresh", "mar_attn_full_select",
     "mar_attn_cache_aware", "mar_attn_cache_aware_gather", "mar_kv_scatter", "mar_kv_gather",
     "mar_refresh_topk", "mar_refresh_topk_pairs", "mar_token_cosine", "mar_select_recompute",
-    "mar_cfg_residual", "mar_status_read", "mar_error_string", "mar_version",
+    "mar_cfg_residual", "mar_status_read", "mar_error_string", "mar_version", "mar_selftest_wait_timeout",
     "MAR_F32", "MAR_BF16", "MAR_CFG_APPLY", "MAR_CFG_UPDATE",
-    "MAR_STATUS_INDEX_RANGE", "MAR_STATUS_INDEX_DUP",
+    "MAR_STATUS_INDEX_RANGE", "MAR_STATUS_INDEX_DUP", "MAR_STATUS_TIMEOUT",
 ]
 
 MAR_F32, MAR_BF16 = 0, 1
 MAR_CFG_APPLY, MAR_CFG_UPDATE = 0, 1
-MAR_STATUS_INDEX_RANGE, MAR_STATUS_INDEX_DUP = 0x1, 0x2
+MAR_STATUS_INDEX_RANGE, MAR_STATUS_INDEX_DUP, MAR_STATUS_TIMEOUT = 0x1, 0x2, 0x4
 
 _lib = None
 
@@ -85,6 +85,7 @@ def load(path: str | None = None):
         "mar_status_read": ([P, P, P], ctypes.c_int),
         "mar_noalloc_scratch_bytes": ([], SZ),
         "mar_attn_full_noalloc": ([SP, P, P, P, P, F, P, I32, P, P, P, P], ctypes.c_int),
+        "mar_selftest_wait_timeout": ([ctypes.c_uint32, P, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -352,3 +353,11 @@ def mar_status_read(status, stream=None) -> int:
     rc = load().mar_status_read(_ptr(status), ctypes.byref(out), _stream(stream))
     _check("mar_status_read", rc)
     return int(out.value)
+
+
+def mar_selftest_wait_timeout(spin_limit: int, status, stream=None):
+    """Diagnostic: a kernel waits on a barrier that never completes, with the bounded wait of
+    the tensor-core kernels limited to ``spin_limit`` polls; it sets MAR_STATUS_TIMEOUT in
+    ``status`` and returns."""
+    rc = load().mar_selftest_wait_timeout(int(spin_limit), _ptr(status), _stream(stream))
+    _check("mar_selftest_wait_timeout", rc)

@@ -80,7 +80,8 @@ int mar_version(void) { return 10000; }
 
 // Score scratch: with the tcgen05 attention (bf16, d = 64 or 80), G <= 32 and N % 4 == 0 the attention
 // launch leaves the generating rows' raw scores (fp32 [B*H, G, N]) for a small reduction;
-// otherwise a separate score kernel keeps per-head fp64 partials ([B*H, N]).
+// otherwise a separate score launch computes the score, which needs scratch only with more
+// than 16 heads (per-head fp64 partials [B*H, N]; up to 16 heads it sums in a cluster).
 static constexpr int kMaxFusedG = 32;
 static bool fused_score_shape(const mar_shape *s, int32_t G) {
     if (s->dtype != MAR_BF16 || G <= 0 || G > kMaxFusedG || (long long)s->H * G * 16 > 40 * 1024 || (s->N & 3))
@@ -92,7 +93,9 @@ static bool fused_score_shape(const mar_shape *s, int32_t G) {
 static size_t ws_rows(const mar_shape *s, int32_t G) {  // raw scores, then (m, l) per row
     return round_up(sizeof(float) * (size_t)s->B * s->H * G * s->N) + round_up(sizeof(float) * 2 * s->B * s->H * G);
 }
-static size_t ws_partials(const mar_shape *s) { return round_up(sizeof(double) * (size_t)s->B * s->H * s->N); }
+static size_t ws_partials(const mar_shape *s) {
+    return mar::score_uses_partials(s->H) ? round_up(sizeof(double) * (size_t)s->B * s->H * s->N) : 0;
+}
 
 size_t mar_attn_full_workspace_bytes(const mar_shape *s, int32_t G, int want_score) {
     if (check_shape(s) != MAR_OK || !want_score || G <= 0) return 0;
@@ -132,7 +135,8 @@ static int attn_full_core(const mar_shape *s, const void *Q, const void *K, cons
     // else the per-head partials of the separate score kernel
     const bool ws_ok = workspace && !(reinterpret_cast<uintptr_t>(workspace) % kWsAlign);
     const bool fused = want_score && fused_score_shape(s, G) && ws_ok && workspace_bytes >= ws_rows(s, G);
-    if (want_score && !fused && (!ws_ok || workspace_bytes < ws_partials(s))) return MAR_ERR_WORKSPACE;
+    const size_t need_partials = ws_partials(s);
+    if (want_score && !fused && need_partials && (!ws_ok || workspace_bytes < need_partials)) return MAR_ERR_WORKSPACE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
     mar::AttnParams p{};
@@ -155,7 +159,7 @@ static int attn_full_core(const mar_shape *s, const void *Q, const void *K, cons
     } else if (want_score) {
         mar::ScoreParams sp{};
         sp.Q = Q; sp.K = K; sp.gen = gen_idx;
-        sp.partial = static_cast<double *>(workspace);
+        sp.partial = need_partials ? static_cast<double *>(workspace) : nullptr;
         sp.score = score_out; sp.status = d_status;
         sp.B = s->B; sp.H = s->H; sp.N = s->N; sp.d = s->d; sp.G = G;
         sp.bf16 = s->dtype == MAR_BF16;
@@ -250,6 +254,7 @@ int mar_attn_full_refresh(const mar_shape *s, const void *Q, const void *K, cons
     return rows_common(s, s->N, 2, src, dst, nullptr, 1, d_status, stream);
 }
 
+// The cache-aware kernels need no scratch; the workspace arguments are reserved.
 size_t mar_attn_cache_aware_workspace_bytes(const mar_shape *s, int32_t A) {
     (void)s;
     (void)A;

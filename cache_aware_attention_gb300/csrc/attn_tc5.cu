@@ -202,7 +202,8 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
     unsigned char *sm = reinterpret_cast<unsigned char *>(base);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::oBars);
     uint64_t *kv_empty = bars + KV_FULL + S;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + KV_FULL + 2 * S);
+    uint64_t *drain = bars + KV_FULL + 2 * S;  // [2] abort path: the S and the PV issuer's MMAs
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + KV_FULL + 2 * S + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const int bm_words = 2 * ((p.N + BN - 1) / BN);  // one bitmap: whole 64-position blocks
     uint32_t *bitmaps = reinterpret_cast<uint32_t *>(tmem_slot + 4);  // [2][bm_words]
@@ -238,6 +239,8 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             mbar_init(&bars[KV_FULL + i], 1);
             mbar_init(&kv_empty[i], 1);
         }
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
         mbar_fence_init();
     }
     tc_fence_before();
@@ -289,6 +292,9 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             };
             bool ok = true;
             uint32_t done_phase = 0;  // fresh mode: bit st = parity of the next DENSE_DONE[st] phase
+            // abort path: per stage (bits 2st, 2st+1) and per Q buffer whether a TMA load was
+            // issued into it and the barrier parity of the latest one (bit 1: issued, bit 0: parity)
+            uint32_t kv_issued = 0, q_issued = 0;
             for (int it = 0; ok && it < my_tiles; ++it) {
                 const int tile = (int)blockIdx.x + it * (int)gridDim.x;
                 const int bh = tile / nqt, q0 = (tile % nqt) * BM;
@@ -301,6 +307,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                     mbar_arrive_expect_tx(&bars[Q_FULL + qb], C::kQa + C::kQb);
                     tma_load_3d(sq, &P.mQa, 0, q0, bh, &bars[Q_FULL + qb]);
                     if constexpr (C::DB > 0) tma_load_3d(sq + C::kQa, &P.mQb, 64, q0, bh, &bars[Q_FULL + qb]);
+                    q_issued = (q_issued & ~(3u << (2 * qb))) | ((2u | ((it >> 1) & 1)) << (2 * qb));
                 }
                 for (int j = 0; j < nblk; ++j) {
                     const int g = it * nblk + j, st = g % S;
@@ -330,6 +337,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                         tma_load_3d(stg + C::sKb, dense ? &P.mKb : &P.mKcb, 64, row, bh, fb);
                         tma_load_3d(stg + C::sVb, dense ? &P.mVb : &P.mVcb, 64, row, bh, fb);
                     }
+                    kv_issued = (kv_issued & ~(3u << (2 * st))) | ((2u | ((g / S) & 1)) << (2 * st));
                     if (P.store) {
                         if (!(ok = store_pending())) break;
                         bulk_commit_group();
@@ -350,6 +358,16 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             // every store has read its shared-memory source before the CTA exits (the writes
             // themselves are visible to later launches at grid completion)
             bulk_wait_group_read<0>();
+            if (*abort_flag) {
+                // Abort path: the loads already issued still write into the stages and Q
+                // buffers; wait (bounded) until each has landed before the CTA releases its
+                // shared memory. A load's phase is the latest one of its barrier, so the
+                // parity wait is exact.
+                for (int i = 0; i < S; ++i)
+                    if ((kv_issued >> (2 * i)) & 2u) mbar_wait_drain(&bars[KV_FULL + i], (kv_issued >> (2 * i)) & 1u);
+                for (int i = 0; i < 2; ++i)
+                    if ((q_issued >> (2 * i)) & 2u) mbar_wait_drain(&bars[Q_FULL + i], (q_issued >> (2 * i)) & 1u);
+            }
         }
         __syncwarp();
     } else if (warp == 5) {
@@ -362,16 +380,16 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
         const int total = my_tiles * nblk;
         for (int g = 0; g < total; ++g) {
             const int it = g / nblk, j = g - it * nblk;
-            if (!mbar_wait(&bars[KV_FULL + g % S], (g / S) & 1, p.status, abort_flag)) break;
-            if (j == 0 && !mbar_wait(&bars[Q_FULL + (it & 1)], (it >> 1) & 1, p.status, abort_flag)) break;
-            if (g >= SB && !mbar_wait(&bars[O_DONE + g % SB], (g / SB - 1) & 1, p.status, abort_flag)) break;
+            if (!mbar_wait_all(&bars[KV_FULL + g % S], (g / S) & 1, p.status, abort_flag)) break;
+            if (j == 0 && !mbar_wait_all(&bars[Q_FULL + (it & 1)], (it >> 1) & 1, p.status, abort_flag)) break;
+            if (g >= SB && !mbar_wait_all(&bars[O_DONE + g % SB], (g / SB - 1) & 1, p.status, abort_flag)) break;
             tc_fence_after();
             if (j >= nd) {
                 // A cache block: its rows at active positions are stale. Their P will be 0, but
                 // 0 x NaN is NaN, so their V rows are cleared in shared memory here, before S
                 // is issued (PV_g, which reads them, follows S_g through the softmax warps'
                 // hand-over). Whole rows are cleared, so the swizzle inside a row does not matter.
-                if (j == nd && !mbar_wait(&bars[BM_FULL + (it & 1)], (it >> 1) & 1, p.status, abort_flag)) break;
+                if (j == nd && !mbar_wait_all(&bars[BM_FULL + (it & 1)], (it >> 1) & 1, p.status, abort_flag)) break;
                 const uint32_t *bm = bitmaps + (it & 1) * bm_words;
                 const int pos0 = (j - nd) * BN;
                 uint64_t stale = (uint64_t)bm[pos0 >> 5] | ((uint64_t)bm[(pos0 >> 5) + 1] << 32);
@@ -408,6 +426,13 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             __syncwarp();
         }
         __syncwarp();
+        if (*abort_flag) {  // abort path: this warp's MMAs still write tensor memory; wait for them
+            if (elect_one()) {
+                mma_commit(&drain[0]);
+                mbar_wait_drain(&drain[0], 0);
+            }
+            __syncwarp();
+        }
     } else if (warp == 7) {
         // ------------------------------------------------------------ PV issuer
         // O += P_g V_g as soon as the softmax warps have written P_g; its commits release
@@ -417,11 +442,11 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
         const uint32_t idOb = idesc_bf16(BM, 16, 0, 1);
         const int total = my_tiles * nblk;
         for (int g = 0; g < total; ++g) {
-            if (!mbar_wait(&bars[P_FULL + g % SB], (g / SB) & 1, p.status, abort_flag)) break;
+            if (!mbar_wait_all(&bars[P_FULL + g % SB], (g / SB) & 1, p.status, abort_flag)) break;
             // V_g landed long ago (S_g needed the same stage); waiting on its barrier phase
             // here orders this thread's reads after the TMA write. The stage cannot have been
             // refilled: that needs this warp's commit below.
-            if (!mbar_wait(&bars[KV_FULL + g % S], (g / S) & 1, p.status, abort_flag)) break;
+            if (!mbar_wait_all(&bars[KV_FULL + g % S], (g / S) & 1, p.status, abort_flag)) break;
             tc_fence_after();
             const int j = g % nblk;
             const unsigned char *stg = sm + C::oStage + (g % S) * C::kStageBytes;
@@ -441,6 +466,13 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             __syncwarp();
         }
         __syncwarp();
+        if (*abort_flag) {  // abort path, as for the S issuer
+            if (elect_one()) {
+                mma_commit(&drain[1]);
+                mbar_wait_drain(&drain[1], 0);
+            }
+            __syncwarp();
+        }
     } else if (warp == 6) {
         // ------------------------------------------------------------ index warp
         // Fresh mode: the active rows of the tile's queries and of its dense key blocks are
@@ -522,7 +554,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
         auto build_bitmap = [&](int it, int b) -> bool {
             const int bb = it & 1;
             uint32_t *bm = bitmaps + bb * bm_words;
-            if (nc > 0 && !mbar_wait(&bars[BM_EMPTY + bb], ((it >> 1) & 1) ^ 1, p.status, abort_flag)) return false;
+            if (nc > 0 && !mbar_wait_all(&bars[BM_EMPTY + bb], ((it >> 1) & 1) ^ 1, p.status, abort_flag)) return false;
             for (int w = lane; w < bm_words; w += 32) bm[w] = 0u;
             __syncwarp();
             uint32_t bad = 0;
@@ -542,7 +574,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
         };
         // fresh mode: this warp owns the Q buffers, so it also stores each tile's staged O
         auto store_o6 = [&](int t) -> bool {
-            if (!mbar_wait(&bars[O_STAGED + (t & 1)], (t >> 1) & 1, p.status, abort_flag)) return false;
+            if (!mbar_wait_all(&bars[O_STAGED + (t & 1)], (t >> 1) & 1, p.status, abort_flag)) return false;
             if (lane == 0) {
                 const int tt = (int)blockIdx.x + t * (int)gridDim.x;
                 const int tbh = tt / nqt, tq0 = (tt % nqt) * BM;
@@ -586,7 +618,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                 }
                 for (int j = 0; j < nd; ++j) {
                     const int g = it * nblk + j, st = g % S;
-                    if (!(ok = mbar_wait(&bars[DENSE_GO + st], (go_phase >> st) & 1, p.status, abort_flag))) break;
+                    if (!(ok = mbar_wait_all(&bars[DENSE_GO + st], (go_phase >> st) & 1, p.status, abort_flag))) break;
                     go_phase ^= 1u << st;
                     unsigned char *stg = sm + C::oStage + st * C::kStageBytes;
                     const bf16 *src[2] = {gK, gV};
@@ -693,9 +725,9 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             for (int j = 0; j < nblk; ++j) {
                 const int g = it * nblk + j, buf = g % SB;
                 if (j == nd && nc > 0 &&
-                    !(ok = mbar_wait(&bars[BM_FULL + (it & 1)], (it >> 1) & 1, p.status, abort_flag)))
+                    !(ok = mbar_wait_all(&bars[BM_FULL + (it & 1)], (it >> 1) & 1, p.status, abort_flag)))
                     break;
-                if (!(ok = mbar_wait(&bars[S_FULL + buf], (g / SB) & 1, p.status, abort_flag))) break;
+                if (!(ok = mbar_wait_all(&bars[S_FULL + buf], (g / SB) & 1, p.status, abort_flag))) break;
                 tc_fence_after();
                 // slots of this block that are keys: dense rows below n_dense; cache rows below
                 // N whose position is not active (active positions hold stale cache rows, whose
@@ -771,7 +803,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                         // O holds the tile's sum over earlier blocks; wait for PV_{g-1} and
                         // scale the rows that raised their max (the others use factor 1).
                         // PV_g, which adds this block, is issued only after P_FULL below.
-                        ok = mbar_wait(&bars[O_DONE + (g - 1) % SB], ((g - 1) / SB) & 1, p.status, abort_flag);
+                        ok = mbar_wait_all(&bars[O_DONE + (g - 1) % SB], ((g - 1) / SB) & 1, p.status, abort_flag);
                         if (ok) {
                             tc_fence_after();
 #pragma unroll
@@ -799,7 +831,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             // issued, so the parity wait is exact; MMAs complete in order, so PV_gl's
             // completion covers all of the tile's PVs.
             const int gl = it * nblk + nblk - 1;
-            if (!(ok = mbar_wait(&bars[O_DONE + gl % SB], (gl / SB) & 1, p.status, abort_flag))) break;
+            if (!(ok = mbar_wait_all(&bars[O_DONE + gl % SB], (gl / SB) & 1, p.status, abort_flag))) break;
             tc_fence_after();
             if (live) {
                 // normalised O, staged as bf16 in this tile's Q buffer (free: the tile's last S
@@ -908,7 +940,7 @@ cudaError_t launch(const AttnParams &p, cudaStream_t s) {
     const long long tiles = (long long)((p.nq + BM - 1) / BM) * bh;
     if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
     P.n_tiles = (int)tiles;
-    size_t smem = 1024 + C::oBars + 8 * (KV_FULL + 2 * C::kStages) + 16;
+    size_t smem = 1024 + C::oBars + 8 * (KV_FULL + 2 * C::kStages + 2) + 16;
     smem += sizeof(uint32_t) * 2 * 2 * ((p.N + BN - 1) / BN);  // two bitmaps
     const bool gen = p.gen != nullptr && !P.gather;
     if (gen && (p.G < 1 || p.G > 32)) return cudaErrorInvalidValue;  // one generating slot per lane

@@ -124,6 +124,38 @@ MAR_DEVINL void df_merge(float &hi, float &lo, float hi2, float lo2) {
     lo = (lo + lo2) + err;
 }
 
+// ---------------------------------------------------------------- exponentials of large arguments
+// A softmax weight is an exponential of a difference of logits. Evaluated as exp(fl(arg)),
+// its relative error is |arg| * 2^-24 from the rounding of the argument alone: 3e-6 at an
+// argument of 50, which the layer-2 score's 1e-6 bound does not allow for peaked rows.
+// These forms carry the argument as an unevaluated fp32 pair (a two-sum for the
+// difference, the FMA residual for the product) and apply the low part as a first-order
+// correction, leaving the exponential's own error (a few ulp) and O(2^-48) terms.
+
+// exp(scale * (a - b)), scale > 0 (the natural-base form of the separate score kernel)
+MAR_DEVINL float exp_scaled_diff(float a, float b, float scale) {
+    const float d = a - b;
+    const float bb = d - a;
+    const float de = (a - (d - bb)) + (-b - bb);      // a - b == d + de exactly
+    const float y = d * scale;
+    const float ye = fmaf(d, scale, -y) + de * scale;  // d * scale == y + residual exactly
+    const float e = expf(y);
+    return fmaf(e, ye, e);
+}
+
+// 2^(s * (c_hi + c_lo) - m) with c_hi + c_lo = scale * log2(e) to about 2^-48 (the base-2
+// form of the raw-score reduction)
+MAR_DEVINL float exp2_fma_acc(float s, float c_hi, float c_lo, float m) {
+    const float th = s * c_hi;
+    const float tl = fmaf(s, c_hi, -th);               // s * c_hi == th + tl exactly
+    const float u = th - m;
+    const float bb = u - th;
+    const float ue = (th - (u - bb)) + (-m - bb);      // th - m == u + ue exactly
+    const float c = ue + fmaf(s, c_lo, tl);
+    const float e = fast_exp2(u);
+    return fmaf(e, c * kLn2, e);
+}
+
 // ---------------------------------------------------------------- active/cached partition
 // Builds, in shared memory, the ascending list of positions of one batch row that are
 // NOT in idx[0..A) (the cached set), using a bitmap of N bits. All threads of the

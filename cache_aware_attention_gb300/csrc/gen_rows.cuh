@@ -1,11 +1,12 @@
 // Layer-2 score from the generating rows the attention launch left behind (raw scores and
-// the (m, l) of each row's online softmax); shared by the reduction kernel and the top-K
-// kernel, which compute identical values.
+// the (m, l) of each row's online softmax), as the reduction kernel computes it.
 //
-// The score of key j is (1/(H G)) sum over rows r = h * G + g of 2^(s_rj * sl2 - m_r) / l_r,
-// summed in a fixed order: the rows are cut into kScoreGroups consecutive groups; a group is
-// summed in row order with two double-float accumulators taking alternate rows (counted from
-// the group's first row), merged at the end; the groups are merged in group order.
+// The score of key j is (1/(H G)) sum over rows r = h * G + g of 2^(s_rj * sl2 - m_r) / l_r
+// (sl2 = scale * log2(e) as an fp32 pair, the exponent argument carried to fp64-grade
+// accuracy by exp2_fma_acc), summed in a fixed order: the rows are cut into kScoreGroups
+// consecutive groups; a group is summed in row order with two double-float accumulators
+// taking alternate rows (counted from the group's first row), merged at the end; the groups
+// are merged in group order.
 #pragma once
 
 #include "common.cuh"
@@ -47,7 +48,7 @@ MAR_DEVINL int score_group_rows(int rows) { return (rows + kScoreGroups - 1) / k
 // kBatch (even) loads in flight; the sums do not depend on kBatch.
 template <int kBatch>
 MAR_DEVINL void score_group_sum(const float *__restrict__ sj, const RowStat *rstat, int rows, int q, int N,
-                                float sl2, float &hi, float &lo) {
+                                float sl2, float sl2_lo, float &hi, float &lo) {
     static_assert(kBatch % 2 == 0, "alternate rows must keep their accumulator across batches");
     const int per = score_group_rows(rows);
     const int r_lo = q * per, r_hi = min(rows, r_lo + per);
@@ -62,8 +63,8 @@ MAR_DEVINL void score_group_sum(const float *__restrict__ sj, const RowStat *rst
         }
 #pragma unroll
         for (int k = 0; k < kBatch; k += 2) {
-            if (st[k].rl != 0.f) df_add(h0, l0, fast_exp2(fmaf(x[k], sl2, -st[k].m)) * st[k].rl);
-            if (st[k + 1].rl != 0.f) df_add(h1, l1, fast_exp2(fmaf(x[k + 1], sl2, -st[k + 1].m)) * st[k + 1].rl);
+            if (st[k].rl != 0.f) df_add(h0, l0, exp2_fma_acc(x[k], sl2, sl2_lo, st[k].m) * st[k].rl);
+            if (st[k + 1].rl != 0.f) df_add(h1, l1, exp2_fma_acc(x[k + 1], sl2, sl2_lo, st[k + 1].m) * st[k + 1].rl);
         }
     }
     df_merge(h0, l0, h1, l1);

@@ -23,8 +23,9 @@ int record_cuda_error(cudaError_t e);
 
 namespace {
 
-// 24 MiB: the per-head fp64 partials of B*H*N <= 3,145,728 (b, h, token) entries
-// (e.g. 512 rows x 16 heads x 320 tokens, or 128 x 16 x 1088).
+// 24 MiB: the raw-score rows of B*H*G*N <= 6,291,456 (b, h, generating query, token)
+// entries (e.g. 64 rows x 12 heads x 4 queries x 320 tokens), or the per-head fp64
+// partials of B*H*N <= 3,145,728 (b, h, token) entries that more than 16 heads need.
 constexpr size_t kScratchBytes = size_t(24) << 20;
 
 static __device__ __align__(256) unsigned char g_score_scratch[kScratchBytes];
@@ -60,14 +61,19 @@ int mar_attn_full_noalloc(const mar_shape *s, const void *Q, const void *K, cons
                           float scale, const int32_t *gen_idx, int32_t G, float *score_out, float *lse_out,
                           uint32_t *d_status, mar_stream_t stream) {
     if (!s) return MAR_ERR_ARG;
-    const size_t need = mar_attn_full_min_workspace_bytes(s, G, score_out != nullptr);
-    if (need > kScratchBytes) return MAR_ERR_SCRATCH_LIMIT;
+    // full: the raw-score form's scratch where it applies; least: what the separate score
+    // launch needs (0 up to 16 heads). mar_attn_full takes the raw-score form whenever the
+    // workspace it is given holds `full`.
+    const bool want = score_out != nullptr;
+    const size_t full = mar_attn_full_workspace_bytes(s, G, want);
+    const size_t least = mar_attn_full_min_workspace_bytes(s, G, want);
+    if (least > kScratchBytes) return MAR_ERR_SCRATCH_LIMIT;
     void *ws = nullptr;
-    if (need) {
+    if (full) {
         cudaError_t e = scratch_ptr(&ws);
         if (e != cudaSuccess) return mar::record_cuda_error(e);
     }
-    return mar_attn_full(s, Q, K, V, O, scale, gen_idx, G, score_out, lse_out, ws, need ? kScratchBytes : 0,
+    return mar_attn_full(s, Q, K, V, O, scale, gen_idx, G, score_out, lse_out, ws, full ? kScratchBytes : 0,
                          d_status, stream);
 }
 

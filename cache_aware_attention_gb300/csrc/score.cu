@@ -9,7 +9,9 @@
 // The refresh set must match an exact evaluation except where two candidates lie within
 // 1e-6 (relative) of each other, so this path is kept well below that error: bf16
 // products are exact in fp32, each dot product accumulates in fp32 in a fixed order,
-// the exponentials use the accurate expf, and every sum over keys, generating queries
+// the exponentials use the accurate expf on an argument carried as an fp32 pair (so that
+// peaked rows, whose tail weights have arguments of -50 and below, keep their relative
+// accuracy; see exp_scaled_diff), and every sum over keys, generating queries
 // and heads is accumulated with fp64-grade accuracy in a fixed order (deterministic,
 // no atomics).
 //
@@ -46,7 +48,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) score_partial_kernel(ScoreParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     double *acc = reinterpret_cast<double *>(smem_raw);          // [N]
-    float *s = reinterpret_cast<float *>(acc + p.N);              // [GCH][N] logits
+    float *s = reinterpret_cast<float *>(acc + p.N);              // [GCH][N] dot products (unscaled)
     float *qs = s + GCH * p.N;                                    // [GCH][D]
     float *stat = qs + GCH * D;                                   // [GCH][2]: max, 1/l
     __shared__ int valid[GCH];
@@ -132,10 +134,11 @@ __global__ void __launch_bounds__(kThreads) score_partial_kernel(ScoreParams p) 
             }
 #pragma unroll
             for (int g = 0; g < GCH; ++g)
-                if (g < gn) s[g * p.N + j] = dot[g] * p.scale;
+                if (g < gn) s[g * p.N + j] = dot[g];
         }
         __syncthreads();
-        // per generating query (one warp each): max and fp64 sum of exponentials
+        // per generating query (one warp each): max and fp64 sum of exponentials (the scale
+        // is positive, so the max of the unscaled dot products is the max logit)
         for (int g = warp; g < gn; g += kWarps) {
             const float *sg = s + g * p.N;
             float mx = -INFINITY;
@@ -143,7 +146,7 @@ __global__ void __launch_bounds__(kThreads) score_partial_kernel(ScoreParams p) 
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
             double l = 0.0;
-            for (int j = lane; j < p.N; j += 32) l += (double)expf(sg[j] - mx);
+            for (int j = lane; j < p.N; j += 32) l += (double)exp_scaled_diff(sg[j], mx, p.scale);
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
             if (lane == 0) {
@@ -155,7 +158,7 @@ __global__ void __launch_bounds__(kThreads) score_partial_kernel(ScoreParams p) 
         for (int j = tid; j < p.N; j += kThreads) {
             double a = acc[j];
             for (int g = 0; g < gn; ++g)
-                if (valid[g]) a += (double)(expf(s[g * p.N + j] - stat[2 * g]) * stat[2 * g + 1]);
+                if (valid[g]) a += (double)(exp_scaled_diff(s[g * p.N + j], stat[2 * g], p.scale) * stat[2 * g + 1]);
             acc[j] = a;
         }
     }
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(256) score_reduce_kernel(ScoreParams p) {
 // ------------------------------------------------------------------------ cluster kernel
 constexpr int kCThreads = 128;   // 4 warps: with <= 80 registers and ~33 KB, 6 CTAs per SM
 constexpr int kCWarps = kCThreads / 32;
-constexpr int kMaxCluster = 16;
+constexpr int kMaxCluster = kScoreMaxClusterHeads;
 constexpr int kQReg = 4;                // generating queries per pass (held in registers)
 constexpr int kBufBytes = 12 * 1024;    // one of two staging buffers for key rows
 
@@ -220,7 +223,7 @@ __global__ void __launch_bounds__(kCThreads, 6) score_cluster_kernel(ScoreParams
     T *kbuf = reinterpret_cast<T *>(smem_raw);                                          // [2][krows][D]
     float *acc_hi = reinterpret_cast<float *>(smem_raw + 2 * (size_t)krows * D * sizeof(T));  // [N]
     float *acc_lo = acc_hi + p.N;                                                       // [N]
-    float *s = acc_lo + p.N;                                      // [kQReg][N] logits
+    float *s = acc_lo + p.N;                                      // [kQReg][N] dot products (unscaled)
     __shared__ float stat[kQReg][2];                              // max, 1/l
     __shared__ int valid[kQReg];
     __shared__ __align__(8) uint64_t kbar[2];
@@ -318,14 +321,15 @@ __global__ void __launch_bounds__(kCThreads, 6) score_cluster_kernel(ScoreParams
 #pragma unroll
                         for (int cc = 1; cc < CH; ++cc) tot += __shfl_sync(0xffffffffu, part, (base + cc) & 31);
                     }
-                    if (g < gn && lane_used && c == 0 && jl < nr) s[g * p.N + r0 + jl] = tot * p.scale;
+                    if (g < gn && lane_used && c == 0 && jl < nr) s[g * p.N + r0 + jl] = tot;
                 }
             }
             __syncthreads();  // buffer u & 1 consumed
             if (tid == 0 && u + 2 < nuse && !abort_flag) stage(u + 2);
         }
-        // per generating query (one warp each): max, then the double-float sum of the
-        // exponentials (lane-strided in key order, then a butterfly over the lanes)
+        // per generating query (one warp each): max (of the unscaled dot products: the scale
+        // is positive), then the double-float sum of the exponentials (lane-strided in key
+        // order, then a butterfly over the lanes)
         for (int g = warp; g < gn; g += kCWarps) {
             const float *sg = s + g * p.N;
             float mx = -INFINITY;
@@ -333,7 +337,7 @@ __global__ void __launch_bounds__(kCThreads, 6) score_cluster_kernel(ScoreParams
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
             float hi = 0.f, lo = 0.f;
-            for (int j = lane; j < p.N; j += 32) df_add(hi, lo, expf(sg[j] - mx));
+            for (int j = lane; j < p.N; j += 32) df_add(hi, lo, exp_scaled_diff(sg[j], mx, p.scale));
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) {
                 const float h2 = __shfl_xor_sync(0xffffffffu, hi, off), l2 = __shfl_xor_sync(0xffffffffu, lo, off);
@@ -348,7 +352,7 @@ __global__ void __launch_bounds__(kCThreads, 6) score_cluster_kernel(ScoreParams
         for (int j = tid; j < p.N; j += kCThreads) {
             float hi = acc_hi[j], lo = acc_lo[j];
             for (int g = 0; g < gn; ++g)
-                if (valid[g]) df_add(hi, lo, expf(s[g * p.N + j] - stat[g][0]) * stat[g][1]);
+                if (valid[g]) df_add(hi, lo, exp_scaled_diff(s[g * p.N + j], stat[g][0], p.scale) * stat[g][1]);
             acc_hi[j] = hi;
             acc_lo[j] = lo;
         }
@@ -448,7 +452,7 @@ __global__ void __launch_bounds__(kRThreads) score_rows_kernel(const float *__re
                                                                const float2 *__restrict__ gen_ml,
                                                                const int32_t *__restrict__ gen,
                                                                float *__restrict__ score, int H, int G, int N,
-                                                               float sl2) {
+                                                               float sl2, float sl2_lo) {
     extern __shared__ RowStat rstat[];  // [H * G]
     __shared__ float part[2][kScoreGroups][kRKeys];
     const int b = blockIdx.x, rows = H * G, tid = threadIdx.x;
@@ -456,7 +460,7 @@ __global__ void __launch_bounds__(kRThreads) score_rows_kernel(const float *__re
     __syncthreads();
     const int q = tid / kRKeys, kk = tid % kRKeys, j = blockIdx.y * kRKeys + kk;
     float hi = 0.f, lo = 0.f;
-    if (j < N) score_group_sum<8>(gen_s + (int64_t)b * rows * N + j, rstat, rows, q, N, sl2, hi, lo);
+    if (j < N) score_group_sum<8>(gen_s + (int64_t)b * rows * N + j, rstat, rows, q, N, sl2, sl2_lo, hi, lo);
     part[0][q][kk] = hi;
     part[1][q][kk] = lo;
     __syncthreads();
@@ -472,8 +476,11 @@ cudaError_t launch_score_rows(const float *gen_s, const float2 *gen_ml, const in
                               int H, int G, int N, float scale, cudaStream_t s) {
     const size_t smem = sizeof(RowStat) * (size_t)H * G;
     if (smem > 40 * 1024 || B <= 0) return B <= 0 ? cudaSuccess : cudaErrorInvalidValue;
+    // scale * log2(e) as an fp32 pair (hi, lo), formed in double
+    const double c = (double)scale * 1.4426950408889634;
+    const float c_hi = (float)c, c_lo = (float)(c - (double)c_hi);
     score_rows_kernel<<<dim3(B, (N + kRKeys - 1) / kRKeys), kRThreads, smem, s>>>(
-        gen_s, gen_ml, gen, score, H, G, N, scale * 1.4426950408889634f);
+        gen_s, gen_ml, gen, score, H, G, N, c_hi, c_lo);
     return cudaGetLastError();
 }
 
@@ -482,7 +489,7 @@ size_t score_smem_bytes(int N, int d) {
 }
 
 cudaError_t launch_score(const ScoreParams &p, cudaStream_t s) {
-    if (p.H >= 1 && p.H <= kMaxCluster)
+    if (p.H >= 1 && !score_uses_partials(p.H))
         return p.bf16 ? launch_cluster_d<bf16>(p, s) : launch_cluster_d<float>(p, s);
     cudaError_t e = p.bf16 ? launch_partial_d<bf16>(p, s) : launch_partial_d<float>(p, s);
     if (e != cudaSuccess) return e;

@@ -18,6 +18,12 @@ struct ScoreParams {
     float scale;
 };
 
+// Heads per thread-block cluster of the main score kernel. Up to this many heads the
+// head sum runs through distributed shared memory and `partial` is not used; more heads
+// take the two-kernel path, which keeps per-head fp64 partials in the workspace.
+constexpr int kScoreMaxClusterHeads = 16;
+inline bool score_uses_partials(int H) { return H > kScoreMaxClusterHeads; }
+
 size_t score_smem_bytes(int N, int d);
 cudaError_t launch_score(const ScoreParams &p, cudaStream_t s);
 

@@ -11,8 +11,6 @@
 
 #include "common.cuh"
 
-#define MAR_STATUS_TIMEOUT_BIT 0x4u
-
 namespace mar {
 namespace tc5 {
 
@@ -56,14 +54,31 @@ MAR_DEVINL bool mbar_test(uint64_t *bar, uint32_t parity) {
 // records it in *status); *abort (shared) is also raised so other roles can unwind.
 // try_wait costs about 200 cycles even on a phase that has already completed, so a
 // non-blocking test comes first: most waits of a well-fed pipeline find the phase done.
-MAR_DEVINL bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status, volatile int *abort) {
+MAR_DEVINL bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status, volatile int *abort,
+                          uint32_t limit = kSpinLimit) {
     if (mbar_test(bar, parity)) return true;
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    for (uint32_t i = 0; i < limit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if (abort && *abort) return false;
     }
-    report(status, MAR_STATUS_TIMEOUT_BIT);
+    report(status, MAR_STATUS_TIMEOUT);
     if (abort) *abort = 1;
+    return false;
+}
+// mbar_wait by every lane of a warp with one result for all of them: a warp that gives
+// up (a lane timed out, or saw another role's abort) leaves its loop as a whole, so
+// the warp-wide instructions after it (.sync.aligned tensor-memory accesses, elect,
+// shuffles) always run converged.
+MAR_DEVINL bool mbar_wait_all(uint64_t *bar, uint32_t parity, uint32_t *status, volatile int *abort) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort));
+}
+// The same wait on the abort path: it ignores the abort flag (the CTA is unwinding and
+// waits for its own asynchronous copies and MMAs still in flight before it releases the
+// shared and tensor memory they write). Bounded as well; returns false if it gave up.
+MAR_DEVINL bool mbar_wait_drain(uint64_t *bar, uint32_t parity, uint32_t limit = kSpinLimit) {
+    if (mbar_test(bar, parity)) return true;
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
 

@@ -36,7 +36,8 @@
  *  - Device-detected errors set bits in the caller's `d_status` word (a device
  *    uint32 that the caller zeroes; may be NULL to skip reporting): a position
  *    out of [0, N) (all calls that take positions) or repeated within one row
- *    (attention calls). The offending access is skipped and the outputs that
+ *    (attention calls), and a bounded wait inside a kernel that gave up
+ *    (MAR_STATUS_TIMEOUT). The offending access is skipped and the outputs that
  *    depend on it are unspecified. Kernels never trap.
  *  - Returns MAR_OK (0) or a negative mar_result.
  */
@@ -70,6 +71,14 @@ enum mar_result {
 /* Bits OR-ed into *d_status by the kernels. */
 #define MAR_STATUS_INDEX_RANGE 0x1u /* a position outside [0, N) */
 #define MAR_STATUS_INDEX_DUP 0x2u   /* a position repeated within one row */
+/* A wait of the tensor-core attention kernel (on a copy, a tensor-core operation or
+ * another role of the same thread block) ran past its limit of about a second. The
+ * kernel then stops its work, waits (again bounded) for the copies and tensor-core
+ * operations it has already issued, releases its tensor memory and returns: the
+ * outputs of that call are unspecified, the CUDA context stays usable and later calls
+ * are unaffected. It signals a fault of the device or of the library, never a
+ * property of the inputs. */
+#define MAR_STATUS_TIMEOUT 0x4u
 
 enum mar_cfg_mode { MAR_CFG_APPLY = 0, MAR_CFG_UPDATE = 1 };
 
@@ -116,9 +125,11 @@ int mar_version(void);
  *              aligned), or NULL when that size is 0. Contents are overwritten;
  *              calls that overlap on the GPU must not share it. The size is
  *              4*B*H*G*N + 8*B*H*G bytes (each rounded up to 256) where the attention
- *              launch leaves the raw scores, else 8*B*H*N. A workspace of at least
- *              mar_attn_full_min_workspace_bytes() but below the full size is also
- *              accepted: the score is then computed by the separate score launch.
+ *              launch leaves the raw scores; otherwise the separate score launch
+ *              computes the score and needs 8*B*H*N bytes when H > 16, none when
+ *              H <= 16. A workspace of at least mar_attn_full_min_workspace_bytes()
+ *              (possibly 0, i.e. NULL) but below the full size is also accepted: the
+ *              score is then computed by the separate score launch.
  */
 size_t mar_attn_full_workspace_bytes(const mar_shape *shape, int32_t G, int want_score);
 size_t mar_attn_full_min_workspace_bytes(const mar_shape *shape, int32_t G, int want_score);
@@ -175,9 +186,10 @@ int mar_attn_full_refresh(const mar_shape *shape, const void *Q, const void *K, 
  * arguments except the workspace: the score's scratch lives in a buffer compiled into
  * the library (mar_noalloc_scratch_bytes() bytes, 24 MiB, held on every GPU that loads
  * the library until the process exits).
- *  - Returns MAR_ERR_SCRATCH_LIMIT when mar_attn_full_min_workspace_bytes() of the
- *    shape exceeds that buffer (B*H*N above 3,145,728 with a score requested, and
- *    4*B*H*G*N above 24 MiB where the raw-score form applies).
+ *  - Takes the raw-score form of the score when its scratch (see mar_attn_full) fits
+ *    in the buffer, else the separate score launch. Returns MAR_ERR_SCRATCH_LIMIT when
+ *    neither fits: H > 16 with 8*B*H*N bytes above 24 MiB (B*H*N above 3,145,728), and
+ *    the raw-score form not applicable or above 24 MiB as well.
  *  - Allocates nothing. The first call made on a device looks up the buffer's device
  *    address; make that first call before any stream capture.
  *  - All calls share the one buffer: calls that can overlap on the GPU (different
@@ -211,6 +223,10 @@ int mar_attn_full_noalloc(const mar_shape *shape, const void *Q, const void *K, 
  *                      active positions (the mar_kv_scatter update), which no
  *                      query of the call reads.
  *  lse_out             [B,H,A] fp32 or NULL.
+ *  workspace, workspace_bytes
+ *                      reserved: the kernels of this call need no scratch memory
+ *                      (mar_attn_cache_aware_workspace_bytes() returns 0 for every
+ *                      shape); pass NULL and 0. Any value is accepted and ignored.
  *  A == 0 is a no-op. A == N (no cached tokens) is plain attention over K_A.
  *  Limit: N <= 16384.
  */
@@ -365,6 +381,19 @@ int mar_cfg_residual(int32_t mode, int64_t n, const float *cond, float *uncond,
  * (host pointer).
  */
 int mar_status_read(const uint32_t *d_status, uint32_t *h_status, mar_stream_t stream);
+
+/*
+ * mar_selftest_wait_timeout -- exercises the bounded wait of the tensor-core kernels.
+ *
+ * Not part of the method (the pages have no counterpart): a diagnostic for the
+ * status path. One thread block initialises a shared-memory barrier that nothing ever
+ * completes and waits on it with the same bounded wait the attention kernel uses, but
+ * with `spin_limit` polls instead of the kernel's limit of about a second. The wait
+ * gives up, sets MAR_STATUS_TIMEOUT in *d_status and the kernel returns; no copy or
+ * tensor-core operation is in flight. spin_limit must be in [1, 1<<20] (MAR_ERR_ARG
+ * otherwise); d_status must not be NULL.
+ */
+int mar_selftest_wait_timeout(uint32_t spin_limit, uint32_t *d_status, mar_stream_t stream);
 
 #ifdef __cplusplus
 }

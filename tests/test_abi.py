@@ -49,6 +49,21 @@ def test_version_and_error_strings(lib):
     assert mar.mar_version() >= 10000
     for code in range(0, -9, -1):
         assert mar.mar_error_string(code)
+    assert mar.MAR_STATUS_TIMEOUT == 0x4
+
+
+def test_status_bits_match_the_header():
+    text = open(os.path.join(ROOT, "include", "marattn.h")).read()
+    bits = dict(re.findall(r"#define (MAR_STATUS_[A-Z_]+) (0x[0-9a-fA-F]+)u", text))
+    assert bits == {"MAR_STATUS_INDEX_RANGE": "0x1", "MAR_STATUS_INDEX_DUP": "0x2", "MAR_STATUS_TIMEOUT": "0x4"}
+    for name, val in bits.items():
+        assert getattr(mar, name) == int(val, 16)
+
+
+def test_selftest_validation(lib):
+    assert lib.mar_selftest_wait_timeout(0, FAKE, None) == -1          # limit below 1
+    assert lib.mar_selftest_wait_timeout((1 << 20) + 1, FAKE, None) == -1
+    assert lib.mar_selftest_wait_timeout(100, None, None) == -1        # no status word
 
 
 FAKE = 1 << 20  # a 16-byte aligned non-null address that host validation never dereferences
@@ -68,15 +83,19 @@ def test_attn_full_validation(lib):
     assert lib.mar_attn_full(*args(_shape(), q=0)) == -1          # NULL Q
     assert lib.mar_attn_full(*args(_shape(), q=FAKE + 8)) == -4   # misaligned
     assert lib.mar_attn_full(*args(_shape(), score=FAKE, G=0, gen=FAKE)) == -1  # score needs G >= 1
-    # score without workspace
-    assert lib.mar_attn_full(*args(_shape(), score=FAKE, G=4, gen=FAKE)) == -5
     need = lib.mar_attn_full_workspace_bytes(_shape(), 4, 1)
     assert need == 4 * 2 * 2 * 4 * 64 + 256 and need % 256 == 0  # raw-score rows + (m, l) (bf16, d = 64)
-    least = lib.mar_attn_full_min_workspace_bytes(_shape(), 4, 1)
-    assert least == 8 * 2 * 2 * 64                               # per-head partials
-    assert lib.mar_attn_full_workspace_bytes(_shape(d=32), 4, 1) == least   # no raw-score form
-    assert lib.mar_attn_full_workspace_bytes(_shape(), 33, 1) == least      # G above 32
-    assert lib.mar_attn_full(*args(_shape(), score=FAKE, G=4, gen=FAKE, ws=FAKE, wb=least - 1)) == -5
+    # up to 16 heads the separate score launch needs no scratch; with more it keeps fp64
+    # per-head partials
+    assert lib.mar_attn_full_min_workspace_bytes(_shape(), 4, 1) == 0
+    assert lib.mar_attn_full_workspace_bytes(_shape(d=32), 4, 1) == 0       # no raw-score form
+    assert lib.mar_attn_full_workspace_bytes(_shape(), 33, 1) == 0          # G above 32
+    least = lib.mar_attn_full_min_workspace_bytes(_shape(H=20), 4, 1)
+    assert least == 8 * 2 * 20 * 64
+    assert lib.mar_attn_full_workspace_bytes(_shape(H=20, d=32), 4, 1) == least
+    # a score without the scratch it needs (20 heads): rejected before any launch
+    assert lib.mar_attn_full(*args(_shape(H=20), score=FAKE, G=4, gen=FAKE)) == -5
+    assert lib.mar_attn_full(*args(_shape(H=20), score=FAKE, G=4, gen=FAKE, ws=FAKE, wb=least - 1)) == -5
     assert lib.mar_attn_full(*args(_shape(B=0))) == 0             # empty: no-op
 
 

@@ -155,7 +155,7 @@ def test_cache_aware_equals_full_attention_when_cache_current():
     K, V = _rand((B, H, N, d), 41, torch.bfloat16), _rand((B, H, N, d), 42, torch.bfloat16)
     idx = _active(B, A, N, 43)
     Q_A = _rand((B, H, A, d), 44, torch.bfloat16)
-    K_A, V_A = mar.mar_kv_gather([K, V], idx)
+    K_A, V_A = (_gather_host(x, idx).to(DEV).contiguous() for x in (K, V))   # host gathers
     O = mar.mar_attn_cache_aware(Q_A, K_A, V_A, K, V, idx)
     O_ref, _ = oracle.full_attn(Q_A, K, V)
     P.assert_close(O, O_ref, "bf16", "O_A vs full")
@@ -183,9 +183,10 @@ def test_cache_aware_mar_b_full_size():
     idx = torch.cat([ss.gen, ss.just, _active(cfg.Bp, cfg.K, cfg.N, 61)], 1)
     # refresh positions drawn apart from gen/just: rebuild rows that collide
     idx = _distinct_rows(idx, cfg.N, 62)
-    QA, KA, VA = mar.mar_kv_gather([ss.Q3, ss.K3, ss.V3], idx)
+    QA, KA, VA = (_gather_host(x, idx) for x in (ss.Q3, ss.K3, ss.V3))   # host gathers
+    d_ = lambda x: x.to(DEV).contiguous()
     st = _status()
-    O = mar.mar_attn_cache_aware(QA, KA, VA, ss.Kc, ss.Vc, idx, status=st)
+    O = mar.mar_attn_cache_aware(d_(QA), d_(KA), d_(VA), ss.Kc, ss.Vc, idx, status=st)
     assert mar.mar_status_read(st) == 0
     O_ref, _ = oracle.cache_aware(QA, KA, VA, ss.Kc, ss.Vc, idx)
     P.assert_close(O, O_ref, "bf16", "MAR-B O_A")
@@ -486,12 +487,12 @@ def test_score_raw_rows_and_partials_agree(d, N, G):
     full = mar.load().mar_attn_full_workspace_bytes(s, G, 1)
     least = mar.load().mar_attn_full_min_workspace_bytes(s, G, 1)
     up = lambda n: n + (-n) % 256
-    assert least == up(8 * B * H * N)
+    assert least == 0                     # 12 heads: the separate launch sums in a cluster, no scratch
     raw = N % 4 == 0 and G <= 32          # the raw-row form: N % 4 == 0, at most 32 generating queries
-    assert full == (up(4 * B * H * G * N) + up(8 * B * H * G) if raw else least)
+    assert full == (up(4 * B * H * G * N) + up(8 * B * H * G) if raw else 0)
     errs = []
     for nbytes in (full, least):
-        ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV) if nbytes else None
         score = torch.empty(B, N, dtype=torch.float32, device=DEV)
         st = _status()
         mar.mar_attn_full(Q, Kt, V, gen_idx=gen, score_out=score, workspace=ws, status=st)
