@@ -86,8 +86,10 @@ class DecodeStep:
         return buf[: self.B * self.H * A * self.d].view(self.B, self.H, A, self.d)
 
     def run(self, step: int, layer2, layer3, cache, gen: torch.Tensor, exclude: torch.Tensor,
-            stream=None):
+            stream=None, events=None):
         """Run one step. ``layer2``/``layer3`` are (Q, K, V); ``cache`` is (K_cache, V_cache).
+        ``events``: optional (start, end) CUDA events recorded on the stream around the
+        layer-3 call (the cache-aware launch, or the full attention with the cache refresh).
 
         Returns ("full", O3 [B',H,N,d]) on a full-refresh step, else
         ("cached", O_A [B',H,A,d], active [B',A])."""
@@ -97,7 +99,9 @@ class DecodeStep:
         if is_full_refresh(step):
             mar_attn_full(Q2, K2, V2, self.O2, status=self.status, stream=stream)
             # layer 3: full attention and the whole-cache overwrite in one call
+            _record(events, 0, stream)
             mar_attn_full_refresh(Q3, K3, V3, Kc, Vc, self.O3, status=self.status, stream=stream)
+            _record(events, 1, stream)
             return ("full", self.O3)
         K = self.refresh_count(exclude.shape[1])
         A = exclude.shape[1] + K
@@ -113,9 +117,9 @@ class DecodeStep:
             # layer 2: attention, score, refresh set and active set
             mar_attn_full_select(Q2, K2, V2, gen, exclude, K, self.score, O=self.O2, out_idx=self.refresh_set(K),
                                  active_out=act, workspace=self.workspace, status=self.status, stream=stream)
-        return self.cached_layer(A, layer3, cache, stream=stream)
+        return self.cached_layer(A, layer3, cache, stream=stream, events=events)
 
-    def cached_layer(self, A: int, layer3, cache, stream=None):
+    def cached_layer(self, A: int, layer3, cache, stream=None, events=None):
         """Cache-aware attention of layer 3's active rows with the fused cache scatter, using
         the active set already in ``active(A)``: in one launch reading the rows in place, or
         as a gather into dense blocks followed by the attention."""
@@ -124,11 +128,20 @@ class DecodeStep:
         act = self.active(A)
         oa = self.dense(3, A)
         if self.fused_gather:
+            _record(events, 0, stream)
             mar_attn_cache_aware_gather(Q3, K3, V3, Kc, Vc, act, O_A=oa, fuse_scatter=True, status=self.status,
                                         stream=stream)
+            _record(events, 1, stream)
             return ("cached", oa, act)
         qa, ka, va = (self.dense(i, A) for i in range(3))
+        _record(events, 0, stream)
         mar_kv_gather([Q3, K3, V3], act, dsts=[qa, ka, va], status=self.status, stream=stream)
         mar_attn_cache_aware(qa, ka, va, Kc, Vc, act, O_A=oa, fuse_scatter=True, status=self.status,
                              stream=stream)
+        _record(events, 1, stream)
         return ("cached", oa, act)
+
+
+def _record(events, i: int, stream):
+    if events is not None:
+        events[i].record(stream if stream is not None else torch.cuda.current_stream())
