@@ -161,7 +161,7 @@ class InputSet:
                 "gen": pin(self.gen), "exclude": pin(self.exclude), "cond": pin(self.cond)}
 
 
-# Algorithmic bytes (SURVEY-style accounting, bf16 = 2 bytes per element)
+# Algorithmic bytes per call (bf16 = 2 bytes per element)
 def bytes_full_attention(cfg):
     return 4 * cfg.Bp * cfg.H * cfg.N * cfg.d * 2          # Q, K, V read + O write
 
@@ -310,16 +310,17 @@ def run_mine(args, ws, rank, local):
     ca_mean = statistics.fmean(ca_us)
     assert mar.mar_status_read(step.status) == 0, "device reported an index error"
 
-    refresh = refresh_leg(args, cfg, sets, step, mar, is_full_refresh)
-    schedule = schedule_leg(cfg, sets, step, mar, is_full_refresh)
-    brk = breakdown(cfg, sets, step, mar)
-    sweep_a = sweep_active(cfg, sets, step, mar)
-    sweep_k = sweep_refresh_count(cfg, sets, step, mar)
-    e2e = end_to_end(args, cfg, sets, step, mar, cached_t)
+    legs = args.legs != "none"
+    refresh = refresh_leg(args, cfg, sets, step, mar, is_full_refresh) if legs else None
+    schedule = schedule_leg(cfg, sets, step, mar, is_full_refresh) if legs else None
+    brk = breakdown(cfg, sets, step, mar) if legs else None
+    sweep_a = sweep_active(cfg, sets, step, mar) if legs else None
+    sweep_k = sweep_refresh_count(cfg, sets, step, mar) if legs else None
+    e2e = end_to_end(args, cfg, sets, step, mar, cached_t) if legs else None
     clocks.stop()
     del sets
     torch.cuda.empty_cache()
-    px = px512_leg(mar, dev) if not args.no_px512 else None
+    px = px512_leg(mar, dev) if legs and not args.no_px512 else None
 
     peaks = load_peaks()
     hbm = peaks.get("hbm_gbs", 6800.0)
@@ -342,7 +343,8 @@ def run_mine(args, ws, rank, local):
                            else "fallback 6800 GB/s",
             "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, committed capture of "
                               "this kernel build" if traffic else "no capture of this kernel build"}
-    cpu = cpu_baseline(cfg, budget_s=args.cpu_seconds) if (rank == 0 and ws == 1 and not args.no_cpu) else None
+    cpu = cpu_baseline(cfg, budget_s=args.cpu_seconds) if (rank == 0 and ws == 1 and legs and not args.no_cpu) \
+        else None
     line = {
         "metric": METRIC, "value": total_tokens / (ms_max / 1e3), "unit": UNIT, "n_gpus": ws,
         "steps": K, "warmup": W, "ms_per_step": ms_max / K, "higher_is_better": True,
@@ -758,6 +760,8 @@ def main():
     ap.add_argument("--rows", type=int, default=0, help="batch rows B' (default: the config's)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-px512", action="store_true", help="skip the 512 px leg")
+    ap.add_argument("--legs", default="all", choices=["all", "none"],
+                    help="none: only the warm-up and the timed steps (e.g. for a launch list)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--only", default=None,
                     help="profiling aid: run REPS calls of one C-ABI call kind of the step "

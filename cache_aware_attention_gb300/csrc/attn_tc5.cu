@@ -101,7 +101,7 @@ enum Bar {
     BM_FULL = 13,    // [2]
     BM_EMPTY = 15,   // [2]
     O_STAGED = 17,   // [2] the tile's normalised O is in its Q buffer (one arrival per softmax warp)
-    DENSE_DONE = 19, // [S <= 4] fresh mode: the index warp is done reading a dense-block stage
+    DENSE_DONE = 19, // [S <= 4] fresh mode: the index warp is done with a dense-block stage
     DENSE_GO = 23,   // [S] fresh mode: the producer hands a free stage for a dense block to it
     KV_FULL = 27     // [S], then KV_EMPTY [S]
 };
@@ -312,18 +312,17 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                 for (int j = 0; j < nblk; ++j) {
                     const int g = it * nblk + j, st = g % S;
                     if (!(ok = mbar_wait(&kv_empty[st], ((g / S) & 1) ^ 1, p.status, abort_flag))) break;
-                    if (p.fresh) {
-                        // a stage last used by a dense block is free once the index warp has also
-                        // finished reading it (the fused scatter)
-                        if (g >= S && (g - S) % nblk < nd) {
-                            if (!(ok = mbar_wait(&bars[DENSE_DONE + st], (done_phase >> st) & 1, p.status, abort_flag)))
-                                break;
-                            done_phase ^= 1u << st;
-                        }
-                        if (j < nd) {  // the index warp fills this stage and signals it
-                            mbar_arrive(&bars[DENSE_GO + st]);
-                            continue;
-                        }
+                    if (p.fresh && g >= S && (g - S) % nblk < nd) {
+                        // fresh mode: a stage last used by a dense block is free once the index
+                        // warp has also finished with it (it fills the stage and writes the
+                        // fused scatter from it)
+                        if (!(ok = mbar_wait(&bars[DENSE_DONE + st], (done_phase >> st) & 1, p.status, abort_flag)))
+                            break;
+                        done_phase ^= 1u << st;
+                    }
+                    if (p.fresh && j < nd) {  // the index warp fills this stage and signals it
+                        mbar_arrive(&bars[DENSE_GO + st]);
+                        continue;
                     }
                     if (P.store) bulk_wait_group_read<S - 2>();  // the store of block g - S is done reading
                     unsigned char *stg = sm + C::oStage + st * C::kStageBytes;
@@ -485,17 +484,22 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
         const bf16 *gQ = static_cast<const bf16 *>(p.Q);
         const bf16 *gK = static_cast<const bf16 *>(p.Kd);
         const bf16 *gV = static_cast<const bf16 *>(p.Vd);
-        // rows a0 .. a0 + rows - 1 of the active set (rows <= 128, a multiple of 32) of one or
-        // two tensors into part a at da[n] and tail part at db[n]
-        auto copy_rows = [&](const bf16 *const *src, unsigned char *const *da, unsigned char *const *db, int n,
-                             int a0, int rows, int64_t slab, const int32_t *ix) {
-            int pr[4];
+        // positions of the active rows a0 + 32 k + lane (k < 4) of the rows a0 .. a0 + rows - 1
+        // (rows <= 128), -1 past the active set or out of range: loaded once, then passed to
+        // the copies and the scatter by shuffles (a position load inside their loops would
+        // put one global-memory latency on every pass)
+        auto load_pos = [&](const int32_t *ix, int a0, int rows, int (&pr)[4]) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int a = a0 + 32 * k + lane;
                 const int pos = (32 * k < rows && a < p.A) ? __ldg(ix + a) : -1;
                 pr[k] = (pos >= 0 && pos < p.N) ? pos : -1;
             }
+        };
+        // rows a0 .. a0 + rows - 1 of the active set (rows <= 128, a multiple of 32; positions
+        // pr from load_pos) of one or two tensors into part a at da[n] and tail part at db[n]
+        auto copy_rows = [&](const bf16 *const *src, unsigned char *const *da, unsigned char *const *db, int n,
+                             const int (&pr)[4], int rows, int64_t slab) {
             for (int i = 0; i < rows / 4; ++i) {  // four rows per pass: 8 lanes per row
                 const int r = 4 * i + (lane >> 3), c = lane & 7, sel = i >> 3;
                 const int pos = __shfl_sync(0xffffffffu, sel == 0 ? pr[0] : sel == 1 ? pr[1] : sel == 2 ? pr[2] : pr[3],
@@ -515,17 +519,17 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                 }
             }
         };
-        // Fused scatter in fresh mode, from the stage just filled: the real rows of dense block
-        // a0 .. a0 + 63 go to the cache rows at their positions (K and V). The producer refills
-        // the stage only after DENSE_DONE, which follows these reads.
+        // Fused scatter from a stage holding dense block a0 .. a0 + 63 (positions pr from
+        // load_pos): its real rows go to the cache rows at their positions (K and V). The
+        // producer refills the stage only after DENSE_DONE, which follows these reads.
         bf16 *gKc = static_cast<bf16 *>(p.Kc);
         bf16 *gVc = static_cast<bf16 *>(p.Vc);
-        auto scatter_stage = [&](const unsigned char *stg, int a0, int64_t slab, const int32_t *ix) {
+        auto scatter_stage = [&](const unsigned char *stg, int a0, int64_t slab, const int (&pr)[4]) {
             const int nr = min(BN, p.A - a0);
             for (int i = 0; i < (nr + 3) / 4; ++i) {
                 const int r = 4 * i + (lane >> 3), c = lane & 7;
-                const int pos = r < nr ? __ldg(ix + a0 + r) : -1;
-                if (pos < 0 || pos >= p.N) continue;
+                const int pos = __shfl_sync(0xffffffffu, i < 8 ? pr[0] : pr[1], r & 31);
+                if (pos < 0) continue;  // past the active set (r >= nr) or out of range
                 const uint32_t so = (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
                 const int64_t off = (slab + pos) * D + 8 * c;
                 *reinterpret_cast<uint4 *>(gKc + off) = *reinterpret_cast<const uint4 *>(stg + C::sKa + so);
@@ -534,8 +538,8 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             if constexpr (C::DB > 0) {
                 for (int i = 0; i < (nr + 15) / 16; ++i) {
                     const int r = 16 * i + (lane >> 1), c = lane & 1;
-                    const int pos = r < nr ? __ldg(ix + a0 + r) : -1;
-                    if (pos < 0 || pos >= p.N) continue;
+                    const int pos = __shfl_sync(0xffffffffu, i < 2 ? pr[0] : pr[1], r & 31);
+                    if (pos < 0) continue;
                     const uint32_t so = (uint32_t)(r * 32 + ((c ^ ((r >> 2) & 1)) << 4));
                     const int64_t off = (slab + pos) * D + 64 + 8 * c;
                     *reinterpret_cast<uint4 *>(gKc + off) = *reinterpret_cast<const uint4 *>(stg + C::sKb + so);
@@ -614,7 +618,10 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                     unsigned char *sq = sm + C::oQ + qb * C::kQBytes;
                     unsigned char *sqb = sq + C::kQa;
                     // whole warps of query rows (those of a warp with no real row are never read)
-                    copy_rows(&gQ, &sq, &sqb, 1, q0, min(BM, (p.nq - q0 + 31) & ~31), slab, ix);
+                    const int rows = min(BM, (p.nq - q0 + 31) & ~31);
+                    int pq[4];
+                    load_pos(ix, q0, rows, pq);
+                    copy_rows(&gQ, &sq, &sqb, 1, pq, rows, slab);
                 }
                 for (int j = 0; j < nd; ++j) {
                     const int g = it * nblk + j, st = g % S;
@@ -624,7 +631,9 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                     const bf16 *src[2] = {gK, gV};
                     unsigned char *da[2] = {stg + C::sKa, stg + C::sVa};
                     unsigned char *db[2] = {stg + C::sKb, stg + C::sVb};
-                    copy_rows(src, da, db, 2, j * BN, BN, slab, ix);
+                    int pk[4];
+                    load_pos(ix, j * BN, BN, pk);
+                    copy_rows(src, da, db, 2, pk, BN, slab);
                     land();
                     if (lane == 0) {
                         if (j == 0) mbar_arrive(&bars[Q_FULL + qb]);
@@ -633,7 +642,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                     // the bitmap is read from the first cache block on; the positions are
                     // checked even when there is none (A == N)
                     if (j == 0 && !(ok = build_bitmap(it, b))) break;
-                    if (p.fuse_scatter && qt == 0) scatter_stage(stg, j * BN, slab, ix);
+                    if (p.fuse_scatter && qt == 0) scatter_stage(stg, j * BN, slab, pk);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars[DENSE_DONE + st]);
                 }
@@ -648,39 +657,41 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                 const int bh = tile / nqt, qt = tile % nqt, b = bh / p.H;
                 // with no cache blocks (A == N) nothing reads the bitmap
                 if (nc > 0 && !(ok = build_bitmap(it, b))) break;
-                if (p.fuse_scatter && qt == 0) {
-                    // Fresh K_A/V_A rows -> cache rows of the active positions. No query of
-                    // this launch uses those rows (they are masked as stale).
-                    const bf16 *Kd = static_cast<const bf16 *>(p.Kd);
-                    const bf16 *Vd = static_cast<const bf16 *>(p.Vd);
-                    bf16 *Kc = static_cast<bf16 *>(p.Kc);
-                    bf16 *Vc = static_cast<bf16 *>(p.Vc);
-                    // eight 16-byte chunks per lane and pass, all loads before the stores, so
-                    // that the passes are not serialised on the load latency
-                    constexpr int kU = 8;
-                    for (int t0 = 0; t0 < p.A * (D / 8); t0 += 32 * kU) {
+                if (!p.fuse_scatter || qt != 0) continue;
+                // Fresh K_A/V_A rows -> cache rows of the active positions. No query of this
+                // launch uses those rows (they are masked as stale). The rows are copied 32 at a
+                // time: each lane loads one row's position, which the copies take by shuffles;
+                // eight 16-byte chunks per lane and pass, all loads before the stores, so that
+                // the passes are not serialised on the load latency.
+                const bf16 *Kd = static_cast<const bf16 *>(p.Kd);
+                const bf16 *Vd = static_cast<const bf16 *>(p.Vd);
+                constexpr int CH = D / 8;  // 16-byte chunks per row
+                constexpr int kU = 8;
+                for (int a0 = 0; a0 < p.A; a0 += 32) {
+                    const int nr = min(32, p.A - a0);
+                    int posl = lane < nr ? __ldg(p.idx + (int64_t)b * p.A + a0 + lane) : -1;
+                    if (posl >= p.N) posl = -1;
+                    for (int t0 = 0; t0 < nr * CH; t0 += 32 * kU) {
                         uint4 kv[kU], vv[kU];
                         int64_t dst[kU];
 #pragma unroll
                         for (int u = 0; u < kU; ++u) {
                             const int t = t0 + 32 * u + lane;
+                            const int r = t / CH, c = t % CH;
+                            const int pos = __shfl_sync(0xffffffffu, posl, r & 31);
                             dst[u] = -1;
-                            if (t < p.A * (D / 8)) {
-                                const int a = t / (D / 8), c = t % (D / 8);
-                                const int pos = __ldg(p.idx + (int64_t)b * p.A + a);
-                                if (pos >= 0 && pos < p.N) {
-                                    const int64_t src = ((int64_t)bh * p.A + a) * D + 8 * c;
-                                    kv[u] = __ldg(reinterpret_cast<const uint4 *>(Kd + src));
-                                    vv[u] = __ldg(reinterpret_cast<const uint4 *>(Vd + src));
-                                    dst[u] = ((int64_t)bh * p.N + pos) * D + 8 * c;
-                                }
+                            if (t < nr * CH && pos >= 0) {
+                                const int64_t src = ((int64_t)bh * p.A + a0 + r) * D + 8 * c;
+                                kv[u] = __ldg(reinterpret_cast<const uint4 *>(Kd + src));
+                                vv[u] = __ldg(reinterpret_cast<const uint4 *>(Vd + src));
+                                dst[u] = ((int64_t)bh * p.N + pos) * D + 8 * c;
                             }
                         }
 #pragma unroll
                         for (int u = 0; u < kU; ++u)
                             if (dst[u] >= 0) {
-                                *reinterpret_cast<uint4 *>(Kc + dst[u]) = kv[u];
-                                *reinterpret_cast<uint4 *>(Vc + dst[u]) = vv[u];
+                                *reinterpret_cast<uint4 *>(gKc + dst[u]) = kv[u];
+                                *reinterpret_cast<uint4 *>(gVc + dst[u]) = vv[u];
                             }
                     }
                 }
@@ -821,7 +832,11 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&bars[P_FULL + buf]);
+                    // P (and a rescaled O) is in tensor memory, complete after tcgen05.wait::st and
+                    // ordered by the tcgen05 fences: the arrival need not release this thread's
+                    // global stores (the raw scores of a generating row), whose visibility a
+                    // release arrival would wait for on every block
+                    mbar_arrive_relaxed(&bars[P_FULL + buf]);
                     if (j == nblk - 1 && nc > 0) mbar_arrive(&bars[BM_EMPTY + (it & 1)]);
                 }
                 if (!ok) break;

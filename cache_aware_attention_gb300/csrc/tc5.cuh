@@ -26,6 +26,13 @@ MAR_DEVINL void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cl
 MAR_DEVINL void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
 }
+// Arrival with relaxed memory semantics: it orders no earlier memory access of this thread.
+// For hand-overs whose data is in tensor memory (ordered by tcgen05.wait and the tcgen05
+// fences), where a release arrival would also wait for this thread's outstanding global
+// stores to become visible.
+MAR_DEVINL void mbar_arrive_relaxed(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
 MAR_DEVINL void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
@@ -65,28 +72,15 @@ MAR_DEVINL bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status, vola
     if (abort) *abort = 1;
     return false;
 }
-// mbar_wait by every lane of a converged warp with one result for all of them: a warp
-// that gives up (a lane timed out, or saw another role's abort) leaves its loop as a
-// whole, so the warp-wide instructions after it (.sync.aligned tensor-memory accesses,
-// elect, shuffles) always run converged. The first test is one instruction for the whole
-// warp, so its outcome is the same in every lane and needs no vote; only a wait that
-// polls ends with one (a vote on every wait measured 10-20% slower in the attention
-// kernel).
+// mbar_wait by every lane of a warp with one result for all of them: a warp that gives
+// up (a lane timed out, or saw another role's abort) leaves its loop as a whole, so the
+// warp-wide instructions after it (.sync.aligned tensor-memory accesses, elect,
+// shuffles) always run converged. The vote is taken on every wait: a vote only after
+// polling would leave out the lanes whose first test passed (a barrier test need not
+// give every lane the same answer), and single-lane issuer loops, which need no vote,
+// measured 15-35% slower.
 MAR_DEVINL bool mbar_wait_all(uint64_t *bar, uint32_t parity, uint32_t *status, volatile int *abort) {
-    if (mbar_test(bar, parity)) return true;
-    bool ok = false;
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) {
-            ok = true;
-            break;
-        }
-        if (abort && *abort) break;
-    }
-    if (!ok && !(abort && *abort)) {
-        report(status, MAR_STATUS_TIMEOUT);
-        if (abort) *abort = 1;
-    }
-    return __all_sync(0xffffffffu, ok);
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort));
 }
 // The same wait on the abort path: it ignores the abort flag (the CTA is unwinding and
 // waits for its own asynchronous copies and MMAs still in flight before it releases the
