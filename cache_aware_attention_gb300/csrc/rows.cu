@@ -34,7 +34,9 @@ __global__ void __launch_bounds__(kThreads) rows_kernel(RowCopyParams p) {
         if (p.idx) {
             pos = p.idx[(int64_t)b * p.A + a];
             if (pos < 0 || pos >= p.N) {
-                if (tensor == 0 && c == 0) report(p.status, MAR_STATUS_INDEX_RANGE);
+                // -1 pads a row of positions (as the recompute set is written); anything
+                // else outside [0, N) is an error
+                if (pos != -1 && tensor == 0 && c == 0) report(p.status, MAR_STATUS_INDEX_RANGE);
                 continue;
             }
         }

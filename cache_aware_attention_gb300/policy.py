@@ -7,7 +7,7 @@ from __future__ import annotations
 
 import torch
 
-from . import mar_attn_cache_aware, mar_kv_scatter, mar_select_recompute, mar_token_cosine
+from . import mar_attn_cache_aware, mar_kv_gather, mar_kv_scatter, mar_select_recompute, mar_token_cosine
 
 
 class TokenCache:
@@ -45,6 +45,14 @@ class TokenCache:
         """A full-compute step: the cache takes every token's feature."""
         mar_kv_scatter(feat, None, None, self.cached, None, stream=stream)
 
+    def update(self, feat: torch.Tensor, idx: torch.Tensor, work: torch.Tensor, stream=None):
+        """A reuse step: the recomputed tokens' features (rows ``idx`` [B, N] of ``feat``,
+        padded with -1 as ``recompute_set`` returns them) replace their cached rows.
+        ``work`` is a dense buffer of the cache's shape: the rows are gathered into it and
+        scattered from it (two row-copy launches; -1 slots are skipped)."""
+        mar_kv_gather([feat], idx, dsts=[work], stream=stream)
+        mar_kv_scatter(work, None, idx, self.cached, None, stream=stream)
+
 
 def kv_drift(K_cache: torch.Tensor, K_fresh: torch.Tensor, V_cache: torch.Tensor, V_fresh: torch.Tensor,
              stream=None):
@@ -54,12 +62,12 @@ def kv_drift(K_cache: torch.Tensor, K_fresh: torch.Tensor, V_cache: torch.Tensor
             mar_token_cosine(V_cache, V_fresh, stream=stream))
 
 
-def stale_attention_error(Q_A, K_A, V_A, cache, fresh, active, stream=None) -> float:
-    """Relative error ||O_stale - O_fresh|| / ||O_fresh|| of the active queries' cache-aware
-    attention over the stale cache against the same attention over a current cache (which,
-    by the MARché Appendix A equivalence, equals full attention over the fresh K/V): what a
-    refresh recovers. ``cache`` and ``fresh`` are (K, V) pairs [B, H, N, d]."""
+def stale_and_current_outputs(Q_A, K_A, V_A, cache, fresh, active, stream=None):
+    """The active queries' cache-aware attention over the stale cache and over a current
+    one (which, by the MARché Appendix A equivalence, equals full attention over the fresh
+    K/V): their difference is what a refresh recovers. ``cache`` and ``fresh`` are (K, V)
+    pairs [B, H, N, d]. Returns (O_stale, O_current) [B, H, A, d]; the caller forms
+    whatever error measure it reports."""
     o_stale = mar_attn_cache_aware(Q_A, K_A, V_A, cache[0], cache[1], active, stream=stream)
-    o_fresh = mar_attn_cache_aware(Q_A, K_A, V_A, fresh[0], fresh[1], active, stream=stream)
-    num = (o_stale.float() - o_fresh.float()).norm()
-    return float(num / o_fresh.float().norm())
+    o_current = mar_attn_cache_aware(Q_A, K_A, V_A, fresh[0], fresh[1], active, stream=stream)
+    return o_stale, o_current

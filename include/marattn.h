@@ -275,8 +275,10 @@ int mar_attn_cache_aware_gather(const mar_shape *shape, int32_t A, const void *Q
  * Either the K pair or the V pair may be NULL to skip that tensor. Repeated
  * positions leave it unspecified which row lands. Row copies (this call and
  * mar_kv_gather) take any d whose row is whole 16-byte vectors, d <= 16384 (e.g. a
- * [B, 1, N, D] hidden state of a token cache); out-of-range positions set
- * MAR_STATUS_INDEX_RANGE and are skipped.
+ * [B, 1, N, D] hidden state of a token cache). A position of -1 marks an unused slot
+ * of a padded row of positions (mar_select_recompute pads its rows that way): the slot
+ * is skipped silently. Any other position outside [0, N) sets MAR_STATUS_INDEX_RANGE
+ * and is skipped.
  */
 int mar_kv_scatter(const mar_shape *shape, int32_t A, const void *K_A, const void *V_A,
                    const int32_t *active_idx, void *K_cache, void *V_cache,
@@ -286,7 +288,8 @@ int mar_kv_scatter(const mar_shape *shape, int32_t A, const void *K_A, const voi
  * mar_kv_gather -- copy the active rows of up to 3 full tensors into dense
  * active blocks (the active-token gather that feeds the fresh projections).
  *   dst[t][b,h,a,:] = src[t][b,h,active_idx[b,a],:]   for t < n_tensors (bit copies)
- * src and dst are HOST arrays of n_tensors (1..3) device pointers.
+ * src and dst are HOST arrays of n_tensors (1..3) device pointers. Positions as for
+ * mar_kv_scatter: the dst rows of -1 slots are left as they were.
  */
 int mar_kv_gather(const mar_shape *shape, int32_t A, int32_t n_tensors,
                   const void *const *src, void *const *dst, const int32_t *active_idx,

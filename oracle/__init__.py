@@ -19,6 +19,9 @@ Parity status of each function (pins live in ``tests/test_oracle_pins.py``):
                      orthogonal), a hand-derived case, zero-vector conventions
   select_recompute   pinned: threshold edge cases (equal to tau, NaN), forced tokens
   topk_pairs         pinned: pair symmetry, numpy lexsort of the fp32 summed scores
+  stale_attention_error
+                     pinned: zero on a current cache (the Appendix A equivalence) and
+                     with every position active, positive and growing with the drift
 """
 from __future__ import annotations
 
@@ -253,3 +256,15 @@ def topk_pairs(score, exclude, K: int) -> np.ndarray:
     ex = _i32(exclude).reshape(B2, -1)
     R = topk(comb.astype(np.float64), ex[:Bp], K)
     return np.concatenate([R, R], 0)
+
+
+def stale_attention_error(Q_A, K_A, V_A, Kc, Vc, K_fresh, V_fresh, idx) -> float:
+    """MARché notes, Background & Motivation and Key Design 3: between full refreshes the
+    cached K/V go stale. The error this leaves in a cached step's output is the relative
+    Frobenius distance between the cache-aware attention of the active queries over the
+    stale cache and full attention of the same queries over the fresh K/V (which is what
+    cache-aware attention over a current cache computes, by the Appendix A equivalence):
+        ||O_stale - O_full||_F / ||O_full||_F    (fp64)."""
+    O_stale, _ = cache_aware(Q_A, K_A, V_A, Kc, Vc, idx)
+    O_full, _ = full_attn(Q_A, K_fresh, V_fresh)
+    return float(np.linalg.norm(O_stale - O_full) / np.linalg.norm(O_full))

@@ -19,7 +19,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import cache_aware, full_attn, gather, l2_score, scatter, topk
+from . import cache_aware, full_attn, gather, l2_score, scatter, select_recompute, token_cosine, topk
 
 REFRESH_EVERY = 3
 
@@ -67,3 +67,50 @@ def _from_bytes(raw: np.ndarray, dtype):
     arr = np.ascontiguousarray(raw).view(view)
     t = torch.from_numpy(arr.copy())
     return t.view(dtype)
+
+
+class OracleTokenCache:
+    """LazyMAR token cache of one layer, followed on the host (notes: Token Cache and the
+    cache-reuse-refresh strategy). The first ``warmup`` steps and every ``period``-th step
+    after them compute every token, and so does every layer below ``shallow_layers``;
+    otherwise a token is recomputed when its feature's cosine similarity to its cached
+    feature is not above ``tau``, or when it is forced (decoded this step), and keeps its
+    cached feature otherwise. The cache is kept as raw bytes [B, 1, N, row_bytes].
+
+    The decision is taken on fp32 similarities (``decide_on``: the values the other side
+    computed, so that both sides decide on the same numbers); the fp64 similarities are
+    returned for the accuracy check."""
+
+    def __init__(self, tau: float, warmup: int, period: int, shallow_layers: int, layer: int):
+        self.tau, self.warmup, self.period = float(tau), warmup, period
+        self.shallow, self.layer = shallow_layers, layer
+        self.cache = None
+
+    def full_compute(self, step: int) -> bool:
+        if self.layer < self.shallow or step < self.warmup:
+            return True
+        return (step - self.warmup) % self.period == 0
+
+    def step(self, t: int, feat, force: np.ndarray, decide_on=None):
+        """``feat`` [B, 1, N, D] torch tensor (CPU); ``force`` [B, F] positions. Returns a
+        dict: kind; for reuse steps cos64 [B, N], idx [B, N] (-1 padded), count [B]."""
+        if self.cache is None or self.full_compute(t):
+            self.cache = _rows(feat).copy()
+            return {"kind": "full"}
+        cached = _from_bytes(self.cache, feat.dtype)
+        cos64 = token_cosine(feat, cached)
+        cos32 = cos64.astype(np.float32) if decide_on is None else np.asarray(decide_on, np.float32)
+        idx, cnt = select_recompute(cos32, self.tau, force)
+        rows = _rows(feat)
+        for b in range(idx.shape[0]):
+            sel = idx[b, :cnt[b]]
+            self.cache[b, :, sel] = rows[b, :, sel]
+        return {"kind": "reuse", "cos64": cos64, "idx": idx, "count": cnt}
+
+
+def _rows(x) -> np.ndarray:
+    """A torch tensor [..., D] as raw bytes [..., row_bytes] (bit copy)."""
+    import torch
+    x = x.detach().to("cpu").contiguous()
+    view = {2: torch.int16, 4: torch.int32}[x.element_size()]
+    return x.view(view).numpy().view(np.uint8).reshape(*x.shape[:-1], -1)

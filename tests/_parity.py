@@ -67,3 +67,40 @@ def topk_mismatches(got: np.ndarray, want: np.ndarray, score64: np.ndarray, excl
                 f"row {b}: position {j} differs and is not a near-tie (gap {gap:.3g}, K-th {thr:.6g})")
             ties.append((b, j, gap / abs(thr)))
     return ties
+
+
+# Sentinel bit patterns for the guard regions around outputs: a NaN payload no kernel
+# writes (bf16, fp32) and an arbitrary word (int32).
+_GUARD = {2: 0x7FC1, 4: 0x7FC0A5A5}
+
+
+def guarded(shape, dtype, device="cuda", guard_bytes: int = 4096, fill=None):
+    """A contiguous tensor of ``shape`` carved from a larger buffer whose ``guard_bytes``
+    before and after it hold a sentinel bit pattern (the tensor starts 4096 bytes into a
+    256-byte aligned allocation, so its own alignment is what a plain allocation gives).
+    ``fill``: initial contents (default: the sentinel too, so that unwritten elements can
+    be found). Returns (tensor, check); check(what) asserts that both guard regions still
+    hold the sentinel."""
+    el = torch.empty((), dtype=dtype).element_size()
+    n = int(np.prod(shape))
+    g = guard_bytes // el
+    buf = torch.empty(n + 2 * g, dtype=dtype, device=device)
+    raw = buf.view({2: torch.int16, 4: torch.int32}[el])
+    pat = _GUARD[el]
+    pat = pat - (1 << 32) if el == 4 and pat >= 1 << 31 else pat
+    raw.fill_(pat)
+    t = buf[g:g + n].view(shape)
+    if fill is not None:
+        t.copy_(fill)
+
+    def check(what: str = ""):
+        torch.cuda.synchronize()
+        assert bool((raw[:g] == pat).all()), f"{what}: written before the tensor's first element"
+        assert bool((raw[g + n:] == pat).all()), f"{what}: written past the tensor's last element"
+
+    def untouched() -> torch.Tensor:
+        """Elements of the tensor that still hold the sentinel (never written)."""
+        return raw[g:g + n].view(shape) == pat
+
+    check.untouched = untouched
+    return t, check

@@ -1,13 +1,29 @@
-"""GPU parity over a whole decode loop: MAR-L shape (batch 128 doubled to 256, 16 heads,
-d=64, 320 tokens), 64 steps with the cosine schedule, top-32 refresh, full refresh every
-3 steps and per-step drift N(0, 0.05) of the fresh Q/K/V.
+"""GPU parity over whole decode loops, and checkpoint/resume of a loop.
 
-The GPU runs the whole batch through ``DecodeStep``; the oracle follows three sampled
-rows with its own cache (rows are independent). After every step: outputs within the
-bf16 tolerance, refresh sets exact (a near-tie within 1e-6 relative is logged and the
-GPU row then takes the oracle's set so the two stay comparable), and the sampled rows of
-the GPU cache bit-identical to the oracle's.
+Loops (64 steps, the cosine schedule, full refresh every 3 steps, per-step drift
+N(0, 0.05) of the fresh Q/K/V):
+  * MAR-L shape: batch 128 doubled to 256, 16 heads, d = 64, 320 tokens, top-32 refresh,
+    in both forms of the cached layer (one launch reading the active rows in place, and
+    gather + cache-aware attention);
+  * 512 px shape: batch 64 doubled to 128, 16 heads, d = 80, 32x32 + 64 = 1088 tokens,
+    top-64 refresh (up to 25 + 25 + 64 active tokens);
+  * MAR-H shape at a reduced batch: 32 doubled to 64, 16 heads, d = 80, 320 tokens,
+    top-64 refresh.
+
+The GPU runs the whole batch through ``DecodeStep``; the oracle follows sampled rows with
+its own cache (rows are independent). After every step: outputs within the bf16
+tolerance, refresh sets exact (a near-tie within 1e-6 relative is logged and the GPU row
+then takes the oracle's set so the two stay comparable), and the sampled rows of the GPU
+cache bit-identical to the oracle's.
+
+Checkpoint/resume: the MAR-L loop's state (the layer-3 cache and the drift streams) is
+saved at step 30, every tensor is dropped, the state is restored into fresh tensors and
+the loop continues; every later step's output and the final cache are bit-identical to
+those of the uninterrupted run (the library keeps no state between calls).
 """
+import hashlib
+import io
+
 import numpy as np
 import pytest
 import torch
@@ -21,6 +37,12 @@ from oracle.loop import OracleRows
 
 pytestmark = pytest.mark.gpu
 
+LOOPS = {
+    "mar_l": workloads.CONFIGS["mar_l_loop"],
+    "px512": workloads.CONFIGS["px512"],
+    "mar_h": workloads.CONFIGS["mar_h"].scaled(B=32, K=64, G=0, J=0, steps=64),
+}
+
 
 def _schedule(cfg):
     """Per-image generation orders and per-step generating positions (host)."""
@@ -33,23 +55,29 @@ def _schedule(cfg):
     return sched, gens
 
 
-@pytest.mark.parametrize("fused_gather", [True, False])
-def test_decode_loop_mar_l(fused_gather):
+def _streams(cfg, dev):
+    shape = (cfg.Bp, cfg.H, cfg.N, cfg.d)
+    return [workloads.DriftStream(shape, cfg.seed * 10_000 + 97 * i, torch.bfloat16, dev, cfg.drift)
+            for i in range(6)]
+
+
+@pytest.mark.parametrize("name,fused_gather", [("mar_l", True), ("mar_l", False), ("px512", True),
+                                               ("mar_h", True)])
+def test_decode_loop(name, fused_gather):
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA device")
-    cfg = workloads.CONFIGS["mar_l_loop"]
+    cfg = LOOPS[name]
     dev = torch.device("cuda")
     sched, gens = _schedule(cfg)
     assert sum(sched) == cfg.n_img and min(sched) >= 1
+    streams = _streams(cfg, dev)
     shape = (cfg.Bp, cfg.H, cfg.N, cfg.d)
-    streams = [workloads.DriftStream(shape, cfg.seed * 10_000 + 97 * i, torch.bfloat16, dev, cfg.drift)
-               for i in range(6)]
     Kc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
     Vc = torch.zeros_like(Kc)
     a_max = 2 * max(sched) + cfg.K
     step = DecodeStep(cfg.Bp, cfg.H, cfg.N, cfg.d, cfg.K, a_max, device=dev, max_gen=max(sched),
                       fused_gather=fused_gather)
-    rows = [0, cfg.B, cfg.Bp - 1]
+    rows = [0, cfg.B, cfg.Bp - 1] if name != "px512" else [0, cfg.Bp - 1]
     orc = OracleRows(rows, cfg.K)
     ties, checked = [], 0
     for t in range(cfg.steps):
@@ -93,3 +121,61 @@ def test_decode_loop_mar_l(fused_gather):
     assert checked == cfg.steps
     if ties:
         print(f"near-ties followed: {ties}")
+
+
+def _digest(x: torch.Tensor) -> str:
+    return hashlib.sha256(P.bits(x).tobytes()).hexdigest()
+
+
+def _run(cfg, gens, step, state, t0, t1, dev):
+    """Steps t0 .. t1 - 1 of the loop on ``state`` (Kc, Vc, streams); returns per-step output digests."""
+    Kc, Vc, streams = state
+    out = []
+    for t in range(t0, t1):
+        Q2, K2, V2, Q3, K3, V3 = (s.advance() for s in streams)
+        gen = gens[t].to(dev)
+        just = gens[t - 1].to(dev) if t > 0 else gen[:, :0]
+        excl = torch.cat([gen, just], 1).contiguous()
+        res = step.run(t, (Q2, K2, V2), (Q3, K3, V3), (Kc, Vc), gen, excl)
+        out.append((res[0], _digest(res[1])) + ((_digest(res[2]),) if res[0] == "cached" else ()))
+    return out
+
+
+def test_checkpoint_resume_is_bit_identical():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    cfg = LOOPS["mar_l"]
+    dev = torch.device("cuda")
+    sched, gens = _schedule(cfg)
+    a_max = 2 * max(sched) + cfg.K
+    step = DecodeStep(cfg.Bp, cfg.H, cfg.N, cfg.d, cfg.K, a_max, device=dev, max_gen=max(sched))
+    shape = (cfg.Bp, cfg.H, cfg.N, cfg.d)
+
+    def fresh_state():
+        Kc = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+        return Kc, torch.zeros_like(Kc), _streams(cfg, dev)
+
+    # uninterrupted
+    st = fresh_state()
+    straight = _run(cfg, gens, step, st, 0, cfg.steps, dev)
+    final = (_digest(st[0]), _digest(st[1]))
+    del st
+    # interrupted at step 30: the state goes to bytes, every tensor is dropped
+    st = fresh_state()
+    first = _run(cfg, gens, step, st, 0, 30, dev)
+    buf = io.BytesIO()
+    torch.save({"Kc": st[0].cpu(), "Vc": st[1].cpu(), "next_step": 30,
+                "streams": [(s.x.cpu(), s.step) for s in st[2]]}, buf)
+    del st
+    torch.cuda.empty_cache()
+    buf.seek(0)
+    ck = torch.load(buf)
+    streams = _streams(cfg, dev)
+    for s, (x, k) in zip(streams, ck["streams"]):
+        s.x.copy_(x.to(dev))
+        s.step = k
+    restored = (ck["Kc"].to(dev), ck["Vc"].to(dev), streams)
+    rest = _run(cfg, gens, step, restored, ck["next_step"], cfg.steps, dev)
+    assert first + rest == straight
+    assert (_digest(restored[0]), _digest(restored[1])) == final
+    assert mar.mar_status_read(step.status) == 0

@@ -167,28 +167,102 @@ def test_decode_step_budget_and_shared_pairs():
     assert np.abs(got - O_ref).max() < 2e-2
 
 
-def test_kv_drift_and_stale_attention_error_over_steps():
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_kv_drift_and_stale_attention_error_over_steps(dtype):
     # MARche notes, Figure 1 / Figures 10-11 and Key Design 3: the keys drift from step to
     # step; between refreshes the cache goes stale and the cached path's error grows; a
-    # refresh brings it back to zero.
-    from cache_aware_attention_gb300.policy import kv_drift, stale_attention_error
+    # refresh brings it back to zero. The per-token cosines and both attention outputs are
+    # compared with the oracle; the error is formed on the host from the GPU outputs and
+    # compared with the oracle's fp64 error within the bound the outputs' own tolerances
+    # give: two outputs each within relative Frobenius eps of exact move the ratio by at
+    # most 2 eps (1 + e) (bf16: eps = 5e-3; fp32: eps from the 1e-5 max-abs bound).
+    import _parity as P
+    from cache_aware_attention_gb300.policy import kv_drift, stale_and_current_outputs
+    t_ = torch.bfloat16 if dtype == "bf16" else torch.float32
     B, H, N, d, A = 4, 12, 320, 64, 40
     K = _rand((B, H, N, d), 730, torch.float32)
     V = _rand((B, H, N, d), 731, torch.float32)
-    Kc, Vc = K.to(torch.bfloat16), V.to(torch.bfloat16)
+    Kc, Vc = K.to(t_), V.to(t_)
     errs, coss = [], []
     for t in range(1, 7):
         K = K + 0.05 * _rand((B, H, N, d), 740 + t, torch.float32)
         V = V + 0.05 * _rand((B, H, N, d), 760 + t, torch.float32)
-        Kf, Vf = K.to(torch.bfloat16), V.to(torch.bfloat16)
+        Kf, Vf = K.to(t_), V.to(t_)
         if t % 3 == 0:
             Kc, Vc = Kf.clone(), Vf.clone()              # full refresh
         ck, cv = kv_drift(Kc, Kf, Vc, Vf)
-        coss.append(float(ck.mean()))
+        for got, x, y in ((ck, Kc, Kf), (cv, Vc, Vf)):
+            ref = oracle.token_cosine(x, y)
+            assert np.abs(got.cpu().numpy().astype(np.float64) - ref).max() <= 1e-6
+        coss.append(float(ck.double().mean()))
         idx = workloads.distinct_positions(B, A, 0, N, 780 + t).to(DEV)
-        QA = _rand((B, H, A, d), 790 + t, torch.bfloat16)
+        QA = _rand((B, H, A, d), 790 + t, t_)
         KA, VA = mar.mar_kv_gather([Kf, Vf], idx)
-        errs.append(stale_attention_error(QA, KA, VA, (Kc, Vc), (Kf, Vf), idx))
-    assert errs[2] < 1e-6 and errs[5] < 1e-6             # refreshed at t = 3 and 6: current cache
+        o_stale, o_cur = stale_and_current_outputs(QA, KA, VA, (Kc, Vc), (Kf, Vf), idx)
+        ref_stale, _ = oracle.cache_aware(QA, KA, VA, Kc, Vc, idx)
+        ref_full, _ = oracle.full_attn(QA, Kf, Vf)
+        P.assert_close(o_stale, ref_stale, dtype, f"step {t} stale")
+        P.assert_close(o_cur, ref_full, dtype, f"step {t} current")
+        g_s, g_c = (P.to_np(x).astype(np.float64) for x in (o_stale, o_cur))
+        e_gpu = np.linalg.norm(g_s - g_c) / np.linalg.norm(g_c)
+        e_ref = oracle.stale_attention_error(QA, KA, VA, Kc, Vc, Kf, Vf, idx)
+        eps = P.BF16_REL_FRO if dtype == "bf16" else P.F32_MAX_ABS * np.sqrt(ref_full.size) / np.linalg.norm(ref_full)
+        assert abs(e_gpu - e_ref) <= 2 * eps * (1 + e_ref), (t, e_gpu, e_ref)
+        errs.append(e_ref)
+    assert errs[2] < 1e-12 and errs[5] < 1e-12           # refreshed at t = 3 and 6: current cache
     assert 0 < errs[0] < errs[1] and 0 < errs[3] < errs[4]
     assert coss[2] == pytest.approx(1.0, abs=1e-6) and coss[0] > coss[1] and coss[3] > coss[4]
+
+
+# ------------------------------------------------------------------------------ LazyMAR token cache
+def test_token_cache_loop_against_the_oracle():
+    # LazyMAR notes, Token Cache and the cache-reuse-refresh strategy, over 16 steps of one
+    # shallow and one deep layer's feature cache [B, 1, N, D]: warm-up steps and every 5th
+    # step after them compute every token; the shallow layer always does; the deep layer
+    # otherwise recomputes the tokens whose cosine similarity to their cached feature is not
+    # above tau, and the tokens decoded at the step, and reuses the rest. Per step: the
+    # similarities within 1e-6 of fp64, the recompute sets equal to the oracle's decided on
+    # the GPU's fp32 similarities (checked separately against fp64: a decision that differs
+    # from the fp64 one must be a near-tie within 1e-6 of tau), and both caches bit-identical
+    # to the oracle's.
+    from cache_aware_attention_gb300.policy import TokenCache
+    from oracle.loop import OracleTokenCache
+    B, N, D, T, tau = 4, 320, 256, 16, 0.995
+    warmup, period, shallow = 3, 5, 3
+    stream = workloads.TokenDriftStream(B, N, D, seed=990, dtype=torch.bfloat16, device=DEV)
+    caches = {layer: torch.zeros(B, 1, N, D, dtype=torch.bfloat16, device=DEV) for layer in (1, 4)}
+    policies = {layer: TokenCache(caches[layer], tau, warmup=warmup, period=period, shallow_layers=shallow)
+                for layer in (1, 4)}
+    oracles = {layer: OracleTokenCache(tau, warmup, period, shallow, layer) for layer in (1, 4)}
+    work = torch.empty(B, 1, N, D, dtype=torch.bfloat16, device=DEV)
+    st = _status()
+    recomputed, reused_steps, near = [], 0, []
+    for t in range(T):
+        decoded = workloads.distinct_positions(B, 4, 64, N, 1000 + t)
+        feat = stream.advance(decoded)
+        for layer in (1, 4):
+            pol, orc = policies[layer], oracles[layer]
+            if not pol.reuses(t, layer):
+                pol.refresh(feat)
+                assert orc.step(t, feat.cpu(), decoded.numpy())["kind"] == "full"
+            else:
+                idx, cnt = pol.recompute_set(feat, force=decoded.to(DEV))
+                cos32 = mar.mar_token_cosine(feat, pol.cached).cpu().numpy()
+                ref = orc.step(t, feat.cpu(), decoded.numpy(), decide_on=cos32)
+                assert np.abs(cos32.astype(np.float64) - ref["cos64"]).max() <= 1e-6
+                np.testing.assert_array_equal(cnt.cpu().numpy(), ref["count"])
+                np.testing.assert_array_equal(idx.cpu().numpy(), ref["idx"])
+                flip = (ref["cos64"] > tau) != (cos32 > np.float32(tau))
+                for b, n in zip(*np.nonzero(flip)):
+                    assert abs(ref["cos64"][b, n] - tau) <= 1e-6 * tau
+                    near.append((t, int(b), int(n)))
+                pol.update(feat, idx, work)
+                recomputed.append(float(cnt.double().mean()) / N)
+                reused_steps += 1
+            torch.cuda.synchronize()
+            assert np.array_equal(oracle._rows_as_bytes(pol.cached.cpu()), orc.cache), f"step {t} layer {layer}"
+    assert mar.mar_status_read(st) == 0
+    assert reused_steps == 10                         # layer 4: steps 0-2 warm up, 3, 8 and 13 refresh
+    assert 0.02 < min(recomputed) and max(recomputed) < 0.9, recomputed   # the cache is really used
+    if near:
+        print(f"near-ties at tau: {near}")

@@ -427,3 +427,75 @@ def test_topk_pairs_symmetry_and_lexsort(oracle_lib):
         cand = np.setdiff1d(np.arange(N), ex[b])
         order = np.lexsort((cand, -comb[cand]))         # score descending, position ascending
         np.testing.assert_array_equal(R[b], np.sort(cand[order[:K]]))
+
+
+# ------------------------------------------------------------------------------ stale-cache error
+def test_stale_attention_error_is_zero_on_a_current_cache(oracle_lib):
+    # Appendix A equivalence: a current cache makes the cached path full attention
+    g = np.random.default_rng(40)
+    B, H, N, A, d = 2, 3, 40, 9, 16
+    K, V = g.standard_normal((B, H, N, d)), g.standard_normal((B, H, N, d))
+    idx = np.stack([g.permutation(N)[:A] for _ in range(B)]).astype(np.int32)
+    QA = g.standard_normal((B, H, A, d))
+    KA = np.stack([K[b][:, idx[b]] for b in range(B)])
+    VA = np.stack([V[b][:, idx[b]] for b in range(B)])
+    assert oracle_lib.stale_attention_error(QA, KA, VA, K, V, K, V, idx) < 1e-12
+    # every position active: no cached token, whatever the cache holds
+    idx_all = np.stack([g.permutation(N) for _ in range(B)]).astype(np.int32)
+    KA = np.stack([K[b][:, idx_all[b]] for b in range(B)])
+    VA = np.stack([V[b][:, idx_all[b]] for b in range(B)])
+    QA = g.standard_normal((B, H, N, d))
+    junk = g.standard_normal((B, H, N, d)) * 10
+    assert oracle_lib.stale_attention_error(QA, KA, VA, junk, junk, K, V, idx_all) < 1e-12
+
+
+def test_stale_attention_error_grows_with_the_drift(oracle_lib):
+    g = np.random.default_rng(41)
+    B, H, N, A, d = 2, 4, 64, 8, 16
+    Kc, Vc = g.standard_normal((B, H, N, d)), g.standard_normal((B, H, N, d))
+    idx = np.stack([g.permutation(N)[:A] for _ in range(B)]).astype(np.int32)
+    QA = g.standard_normal((B, H, A, d))
+    nK, nV = g.standard_normal((B, H, N, d)), g.standard_normal((B, H, N, d))
+    errs = []
+    for drift in (0.01, 0.05, 0.2):
+        K, V = Kc + drift * nK, Vc + drift * nV
+        KA = np.stack([K[b][:, idx[b]] for b in range(B)])
+        VA = np.stack([V[b][:, idx[b]] for b in range(B)])
+        errs.append(oracle_lib.stale_attention_error(QA, KA, VA, Kc, Vc, K, V, idx))
+    assert 0 < errs[0] < errs[1] < errs[2]
+    # first order in the drift: the error scales about linearly at small drift
+    assert errs[1] / errs[0] == pytest.approx(5.0, rel=0.1)
+
+
+# ------------------------------------------------------------------------------ token-cache loop
+def test_oracle_token_cache_extremes(oracle_lib):
+    # LazyMAR token cache: a threshold no similarity exceeds (tau = 1) recomputes every token,
+    # one every similarity exceeds except exact opposites (tau = -1) recomputes only the forced
+    # tokens; warm-up and refresh steps take every token
+    import torch
+    from oracle.loop import OracleTokenCache
+    B, N, D = 2, 12, 8
+    g = np.random.default_rng(42)
+    feats = [torch.from_numpy(g.standard_normal((B, 1, N, D)).astype(np.float32)) for _ in range(6)]
+    force = np.array([[3], [7]], np.int32)
+    every = OracleTokenCache(1.0, warmup=1, period=3, shallow_layers=2, layer=4)
+    only_forced = OracleTokenCache(-1.0, warmup=1, period=3, shallow_layers=2, layer=4)
+    shallow = OracleTokenCache(-1.0, warmup=1, period=3, shallow_layers=2, layer=1)
+    raw = lambda x: x.numpy().view(np.uint8).reshape(B, 1, N, -1)
+    for t, f in enumerate(feats):
+        r1 = every.step(t, f, force)
+        r2 = only_forced.step(t, f, force)
+        shallow.step(t, f, force)
+        assert np.array_equal(every.cache, raw(f)) and np.array_equal(shallow.cache, raw(f))
+        if t in (0, 1, 4):                       # warm-up and the refresh step
+            assert r1["kind"] == r2["kind"] == "full" and np.array_equal(only_forced.cache, raw(f))
+        else:
+            assert r2["kind"] == "reuse" and list(r2["count"]) == [1, 1]
+            last = raw(feats[1] if t < 4 else feats[4])
+            for b in range(B):
+                for n in range(N):
+                    want = raw(f)[b, 0, n] if n == force[b, 0] else None
+                    if want is not None:
+                        assert np.array_equal(only_forced.cache[b, 0, n], want)
+            # the untouched tokens keep their bytes from the last full step or earlier forcing
+            assert np.array_equal(only_forced.cache[0, 0, 0], last[0, 0, 0])

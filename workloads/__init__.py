@@ -29,7 +29,7 @@ import torch
 __all__ = [
     "MarConfig", "CONFIGS", "normal", "cosine_schedule", "generation_order",
     "gen_positions", "distinct_positions", "SingleStep", "single_step",
-    "DriftStream",
+    "DriftStream", "TokenDriftStream",
 ]
 
 
@@ -230,4 +230,37 @@ class DriftStream:
             noise = torch.randn(self.shape, generator=_generator(self.seed + self.step, self.device),
                                 dtype=torch.float32, device=self.device)
             self.x.add_(noise, alpha=self.drift)
+        return self.x.to(self.dtype)
+
+
+class TokenDriftStream:
+    """Per-step features [B, 1, N, D] of one layer of a token cache.
+
+    Keeps fp32 "true" values X. Each token has its own drift scale s[b, n], drawn once
+    from U[lo, hi]; at every step after the first, X[b, :, n] += s[b, n] * N(0, 1) (the
+    generator seeded with ``seed + step``), and the positions passed to ``advance`` (the
+    tokens decoded at that step) also jump by ``jump`` * N(0, 1). The step's tensor is
+    the single rounding of X to ``dtype``. Tokens whose features move little between
+    steps are the ones a token cache reuses."""
+
+    def __init__(self, B: int, N: int, D: int, seed: int, dtype, device, lo: float = 0.005,
+                 hi: float = 0.3, jump: float = 1.0):
+        self.shape, self.seed, self.dtype, self.device = (B, 1, N, D), seed, dtype, device
+        self.jump, self.step = jump, -1
+        g = _generator(seed + 7_000_000, device)
+        self.scale = lo + (hi - lo) * torch.rand(B, 1, N, 1, generator=g, device=device)
+        self.x = normal(self.shape, seed, torch.float32, device)
+
+    def advance(self, decoded: torch.Tensor | None = None) -> torch.Tensor:
+        """``decoded`` [B, k] int positions that jump at this step (or None)."""
+        self.step += 1
+        if self.step > 0:
+            g = _generator(self.seed + self.step, self.device)
+            noise = torch.randn(self.shape, generator=g, dtype=torch.float32, device=self.device)
+            self.x.add_(noise * self.scale)
+            if decoded is not None and decoded.numel():
+                jump = torch.randn(self.shape, generator=g, dtype=torch.float32, device=self.device)
+                mask = torch.zeros(self.shape[0], 1, self.shape[2], 1, device=self.device)
+                mask.scatter_(2, decoded.to(self.device).long()[:, None, :, None], 1.0)
+                self.x.add_(jump * mask * self.jump)
         return self.x.to(self.dtype)
