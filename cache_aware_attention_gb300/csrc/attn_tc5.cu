@@ -117,6 +117,7 @@ struct Tc5Params {
     AttnParams a;
     int gather;
     int store;               // full attention: store every K/V block of query tile 0 to the cache
+    int idle_scatter;        // the fused scatter is written by the softmax warps without a live row
     int n_tiles;
 };
 
@@ -642,7 +643,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                     // the bitmap is read from the first cache block on; the positions are
                     // checked even when there is none (A == N)
                     if (j == 0 && !(ok = build_bitmap(it, b))) break;
-                    if (p.fuse_scatter && qt == 0) scatter_stage(stg, j * BN, slab, pk);
+                    if (p.fuse_scatter && qt == 0 && !P.idle_scatter) scatter_stage(stg, j * BN, slab, pk);
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars[DENSE_DONE + st]);
                 }
@@ -657,7 +658,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                 const int bh = tile / nqt, qt = tile % nqt, b = bh / p.H;
                 // with no cache blocks (A == N) nothing reads the bitmap
                 if (nc > 0 && !(ok = build_bitmap(it, b))) break;
-                if (!p.fuse_scatter || qt != 0) continue;
+                if (!p.fuse_scatter || qt != 0 || P.idle_scatter) continue;
                 // Fresh K_A/V_A rows -> cache rows of the active positions. No query of this
                 // launch uses those rows (they are masked as stale). The rows are copied 32 at a
                 // time: each lane loads one row's position, which the copies take by shuffles;
@@ -701,6 +702,49 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
         // ------------------------------------------------------------ softmax + epilogue
         const float sl2 = p.scale * kLog2e;
         bool ok = true;
+        // The fused scatter of dense block a0 .. a0 + 63 from its stage by the warps without a
+        // live row (warps first_idle .. 3, T threads): each thread takes every T-th of the
+        // block's (row, 16-byte chunk) pieces, eight at a time, positions loaded first.
+        auto scatter_idle = [&](const unsigned char *stg, int bh, int a0) {
+            constexpr int CH = D / 8;  // 16-byte chunks per row: 8 in part a, then the tail's
+            constexpr int kU = 8;
+            const int first_idle = (p.nq + 31) >> 5;
+            const int t0 = (warp - first_idle) * 32 + lane, T = (4 - first_idle) * 32;
+            const int nr = min(BN, p.A - a0), b = bh / p.H;
+            const int32_t *ix = p.idx + (int64_t)b * p.A + a0;
+            bf16 *Kc = static_cast<bf16 *>(p.Kc);
+            bf16 *Vc = static_cast<bf16 *>(p.Vc);
+            for (int u0 = t0; u0 < nr * CH; u0 += kU * T) {
+                int pos[kU];
+#pragma unroll
+                for (int k = 0; k < kU; ++k) {
+                    const int u = u0 + k * T;
+                    pos[k] = u < nr * CH ? __ldg(ix + u / CH) : -1;
+                }
+#pragma unroll
+                for (int k = 0; k < kU; ++k) {
+                    const int u = u0 + k * T;
+                    if (pos[k] < 0 || pos[k] >= p.N) continue;
+                    const int r = u / CH, c = u - r * CH;
+                    uint32_t sa, sv;
+                    int64_t off;
+                    if (c < 8) {
+                        const uint32_t so = (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+                        sa = C::sKa + so;
+                        sv = C::sVa + so;
+                        off = ((int64_t)bh * p.N + pos[k]) * D + 8 * c;
+                    } else {
+                        const int cb = c - 8;
+                        const uint32_t so = (uint32_t)(r * 32 + ((cb ^ ((r >> 2) & 1)) << 4));
+                        sa = C::sKb + so;
+                        sv = C::sVb + so;
+                        off = ((int64_t)bh * p.N + pos[k]) * D + 64 + 8 * cb;
+                    }
+                    *reinterpret_cast<uint4 *>(Kc + off) = *reinterpret_cast<const uint4 *>(stg + sa);
+                    *reinterpret_cast<uint4 *>(Vc + off) = *reinterpret_cast<const uint4 *>(stg + sv);
+                }
+            }
+        };
         int gpos_next = -1;  // full attention with the score: gen[b, lane] of the next tile
         if constexpr (kGen)
             if (my_tiles > 0)
@@ -828,6 +872,13 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                         }
                     }
                     tmem_wait_st();
+                } else if (P.idle_scatter && j < nd) {
+                    // A warp with no live row (the tile has at most 96 queries, and it is the
+                    // (b, h)'s only tile) writes the fused scatter of this dense block from its
+                    // stage: the fresh K/V rows of the active positions to the cache. The stage
+                    // stays put until the block's PV, which waits for this warp's arrival below.
+                    if (!(ok = mbar_wait_all(&bars[KV_FULL + g % S], (g / S) & 1, p.status, abort_flag))) break;
+                    scatter_idle(sm + C::oStage + (g % S) * C::kStageBytes, bh, j * BN);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -945,6 +996,9 @@ cudaError_t launch(const AttnParams &p, cudaStream_t s) {
         ok = ok && map3<D>(&P.mVa, p.Vd, p.n_dense, bh, 64, BN) && map3<D>(&P.mVb, p.Vd, p.n_dense, bh, tw, BN);
     }
     P.store = (!P.gather && p.store_kv) ? 1 : 0;
+    // a single query tile per (b, h) with at most 96 queries leaves softmax warps without a
+    // live row: they write the fused scatter (in place of the index warp)
+    P.idle_scatter = (P.gather && p.fuse_scatter && p.nq <= 96) ? 1 : 0;
     if (P.gather || P.store) {
         ok = ok && map3<D>(&P.mKca, p.Kc, p.N, bh, 64, BN) && map3<D>(&P.mKcb, p.Kc, p.N, bh, tw, BN);
         ok = ok && map3<D>(&P.mVca, p.Vc, p.N, bh, 64, BN) && map3<D>(&P.mVcb, p.Vc, p.N, bh, tw, BN);

@@ -104,7 +104,7 @@ def _extreme_case(case, B, H, N, A, d, seed):
     rnd = lambda *s, std=1.0: torch.randn(*s, generator=g) * std
     shape = (B, H, N, d)
     Q, K, V, Kc, Vc = rnd(*shape), rnd(*shape), rnd(*shape), rnd(*shape), rnd(*shape)
-    if case == "stale_first_block":
+    if case.startswith("stale_first_block"):
         # every position of the first cache block is active: that block is all stale
         rest = torch.stack([torch.randperm(N - BN, generator=g)[:A - BN] + BN for _ in range(B)])
         idx = torch.cat([torch.arange(BN).repeat(B, 1), rest], 1).to(torch.int32)
@@ -121,14 +121,14 @@ def _extreme_case(case, B, H, N, A, d, seed):
         Q[b][:, pos] = u[b] + 0.25 * rnd(H, A, d)  # every active query close to u
         cached = (~active[b]).nonzero()[:, 0]
         last = int(cached.max())                   # the last cached position: in the last block
-        if case in ("late_dominant", "stale_first_block", "cache_dominates"):
+        if case in ("late_dominant", "stale_first_block", "stale_first_block_64", "cache_dominates"):
             Kc[b][:, last] = 2.0 * u[b, :, 0]      # logit ~ 2 |u|^2 scale, ~23 base-2 units at d = 64
         if case == "cache_dominates":
             some = cached[torch.randperm(len(cached), generator=g)[:12]]
             Kc[b][:, some] = 1.5 * u[b] + 0.1 * rnd(H, len(some), d)
         if case == "active_dominates":
             K[b][:, pos[[1, A // 2]]] = 1.5 * u[b] + 0.1 * rnd(H, 2, d)
-    if case == "stale_first_block":
+    if case.startswith("stale_first_block"):
         for b in range(B):                         # stale rows hold values that must never count
             pos = idx[b].long()
             Kc[b][:, pos] = float("nan")
@@ -137,18 +137,21 @@ def _extreme_case(case, B, H, N, A, d, seed):
     return Q, K, V, Kc, Vc, idx
 
 
-CASES = ["wide", "late_dominant", "cache_dominates", "active_dominates", "stale_first_block"]
+CASES = ["wide", "late_dominant", "cache_dominates", "active_dominates", "stale_first_block",
+         "stale_first_block_64"]
 # cases whose inputs must reach the rescale branch (the active-dominant case must not:
 # its first block already holds the max)
-RESCALES = {"wide", "late_dominant", "cache_dominates", "stale_first_block"}
+RESCALES = {"wide", "late_dominant", "cache_dominates", "stale_first_block", "stale_first_block_64"}
 
 
 @pytest.mark.parametrize("case", CASES)
 @pytest.mark.parametrize("form", ["dense", "gather"])
 @pytest.mark.parametrize("dtype,d", [("bf16", 64), ("bf16", 80), ("bf16", 32), ("f32", 64)])
 def test_cache_aware_softmax_extremes(case, form, dtype, d):
+    # A <= 64 runs key-split tiles (two halves over alternate key blocks); with A = 64 and
+    # the first cache block all active, the second half's first block is entirely stale
     B, H, N = 3, 4, 320
-    A = 70 if case == "stale_first_block" else 40
+    A = {"stale_first_block": 70, "stale_first_block_64": 64}.get(case, 40)
     if dtype == "f32" and case == "wide":
         # logits of standard deviation 16: the fp32 dot products' own rounding (about 1e-5 in
         # the logit) moves the weights of two near-equal maxima by more than the fp32
