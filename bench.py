@@ -235,6 +235,11 @@ def graph_time(fn, n_sets: int, reps: int = 24) -> float:
 # ----------------------------------------------------------------------------- our arm
 def config_from_args(args):
     cfg = workloads.CONFIGS[args.config]
+    if cfg.G == 0:
+        # a decode-loop config: its largest step (the cosine schedule's most generating tokens,
+        # as many just decoded)
+        g = max(workloads.cosine_schedule(cfg.n_img, cfg.steps))
+        cfg = cfg.scaled(G=g, J=g)
     if args.rows:
         cfg = cfg.scaled(B=args.rows // 2 if cfg.cfg else args.rows)
     return cfg
