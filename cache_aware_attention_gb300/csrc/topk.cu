@@ -4,14 +4,14 @@
 // become the refreshing tokens; with the generating and just-decoded (caching) tokens
 // they form the active set. Candidates exclude the generating and just-decoded tokens.
 //
-// One CTA per batch row. Scores map to 32-bit keys that order like the floats
-// (sign-magnitude flip), so the selection is exact on the fp32 values. A candidate j is
-// selected when fewer than K candidates precede it in the order (key desc, position
-// asc). For N <= kRankN each thread counts that rank directly against all candidates
-// in shared memory (one pass, broadcast reads). Larger rows use a 4-pass MSB-first radix
-// select over the keys, which finds the K-th largest value T and how many candidates
-// equal to T are taken (the lowest positions first). Selected positions are written in
-// ascending order by a block-wide prefix sum, so the result is deterministic.
+// Scores map to 32-bit keys that order like the floats (sign-magnitude flip), so the
+// selection is exact on the fp32 values: the K candidates first in the order (key desc,
+// position asc). Rows of up to 1152 scores: one warp per row (topk_warp_kernel below).
+// Longer rows: one CTA per row and a 4-pass MSB-first radix select over the keys, which
+// finds the K-th largest value T and how many candidates equal to T are taken (the lowest
+// positions first); selected positions are written in ascending order by a block-wide
+// prefix sum, so the result is deterministic. (The CTA form also keeps a rank-counting
+// pass for rows up to kRankN, used when the warp form does not apply.)
 #include "common.cuh"
 #include "score.h"
 
@@ -162,6 +162,97 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkParams p) {
     }
 }
 
+// Warp-level form for rows of at most kWarpN scores: one warp per batch row, the row's keys
+// in registers (lane l holds positions l, l + 32, ...). An MSB-first radix select over the
+// 32 key bits finds the K-th largest key T among the candidates: at each bit the warp
+// counts the candidates that match the prefix chosen so far with that bit set (a per-lane
+// count, then a butterfly sum) and keeps the bit if at least the remaining number of
+// picks does. The candidates above T are taken, and of those equal to T the `take` lowest
+// positions; positions are written in ascending order by ballot prefix counts. Exactly
+// the selection of the block form.
+constexpr int kWarpN = 1152;
+constexpr int kWarpsPerCta = 4;
+
+template <int kWarpNPL>  // keys per lane: rows of up to 32 * kWarpNPL scores
+__global__ void __launch_bounds__(32 * kWarpsPerCta) topk_warp_kernel(TopkParams p) {
+    __shared__ uint32_t excl_bits[kWarpsPerCta][kWarpN / 32];
+    const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+    const int b = blockIdx.x * kWarpsPerCta + wi;
+    if (b >= p.B) return;  // whole warps leave together
+    const int N = p.N, b2 = b + p.B;
+    uint32_t *ex = excl_bits[wi];
+    for (int w = lane; w < (N + 31) / 32; w += 32) ex[w] = 0u;
+    __syncwarp();
+    for (int e = lane; e < p.E; e += 32) {
+        const int pos = p.exclude[(int64_t)b * p.E + e];
+        if (p.active) {
+            p.active[(int64_t)b * (p.E + p.K) + e] = pos;  // copied as given
+            if (p.pairs) p.active[(int64_t)b2 * (p.E + p.K) + e] = p.exclude[(int64_t)b2 * p.E + e];
+        }
+        if (pos < 0 || pos >= N) {
+            report(p.status, MAR_STATUS_INDEX_RANGE);
+            continue;
+        }
+        atomicOr(&ex[pos >> 5], 1u << (pos & 31));
+    }
+    __syncwarp();
+    if (p.K == 0) return;
+    uint32_t key[kWarpNPL];
+    uint64_t cand = 0;  // bit i: position lane + 32 i is a candidate
+#pragma unroll
+    for (int i = 0; i < kWarpNPL; ++i) {
+        const int j = lane + 32 * i;
+        key[i] = 0u;
+        if (j < N) {
+            const float sc = p.pairs ? __fadd_rn(p.score[(int64_t)b * N + j], p.score[(int64_t)b2 * N + j])
+                                     : p.score[(int64_t)b * N + j];
+            key[i] = order_key(sc);
+            if (!((ex[i] >> lane) & 1u)) cand |= 1ull << i;
+        }
+    }
+    // radix select: T = the K-th largest candidate key, `take` = how many keys equal to T
+    uint32_t T = 0u;
+    int take = p.K;
+    for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t want = T | (1u << bit);
+        const int sh = bit;  // compare the bits at and above `bit`
+        int c = 0;
+#pragma unroll
+        for (int i = 0; i < kWarpNPL; ++i)
+            c += (((cand >> i) & 1ull) && (key[i] >> sh) == (want >> sh)) ? 1 : 0;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+        if (c >= take) T = want;
+        else take -= c;
+    }
+    // ascending positions: the candidates above T, and the first `take` equal to T
+    const uint32_t lt = (1u << lane) - 1u;
+    int base = 0, eq_base = 0;
+    auto emit = [&](int slot, int j) {
+        if (p.out) p.out[(int64_t)b * p.K + slot] = j;
+        if (p.active) p.active[(int64_t)b * (p.E + p.K) + p.E + slot] = j;
+        if (p.pairs) {
+            if (p.out) p.out[(int64_t)b2 * p.K + slot] = j;
+            if (p.active) p.active[(int64_t)b2 * (p.E + p.K) + p.E + slot] = j;
+        }
+    };
+#pragma unroll
+    for (int i = 0; i < kWarpNPL; ++i) {
+        if (32 * i >= N) break;  // warp-uniform
+        const bool c = (cand >> i) & 1ull;
+        const bool eq = c && key[i] == T;
+        const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
+        const bool sel = c && (key[i] > T || (eq && eq_base + __popc(eqm & lt) < take));
+        eq_base += __popc(eqm);
+        const uint32_t selm = __ballot_sync(0xffffffffu, sel);
+        if (sel) {
+            const int slot = base + __popc(selm & lt);
+            if (slot < p.K) emit(slot, lane + 32 * i);
+        }
+        base += __popc(selm);
+    }
+}
+
 constexpr int kSelectMaxN = 16384;
 
 // Token-cache recompute set (LazyMAR notes, Token Cache): one CTA per row; position j is
@@ -202,7 +293,16 @@ __global__ void __launch_bounds__(kThreads) select_recompute_kernel(SelectParams
 
 cudaError_t launch_topk(const TopkParams &p, cudaStream_t s) {
     if (p.N > kMaxN) return cudaErrorInvalidValue;
-    topk_kernel<<<p.B, kThreads, 0, s>>>(p);
+    if (p.B == 0) return cudaSuccess;
+    const unsigned grid = (unsigned)((p.B + kWarpsPerCta - 1) / kWarpsPerCta);
+    if (p.N <= 320)
+        topk_warp_kernel<10><<<grid, 32 * kWarpsPerCta, 0, s>>>(p);
+    else if (p.N <= 640)
+        topk_warp_kernel<20><<<grid, 32 * kWarpsPerCta, 0, s>>>(p);
+    else if (p.N <= kWarpN)
+        topk_warp_kernel<kWarpN / 32><<<grid, 32 * kWarpsPerCta, 0, s>>>(p);
+    else
+        topk_kernel<<<p.B, kThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 
