@@ -996,9 +996,6 @@ cudaError_t launch(const AttnParams &p, cudaStream_t s) {
         ok = ok && map3<D>(&P.mVa, p.Vd, p.n_dense, bh, 64, BN) && map3<D>(&P.mVb, p.Vd, p.n_dense, bh, tw, BN);
     }
     P.store = (!P.gather && p.store_kv) ? 1 : 0;
-    // a single query tile per (b, h) with at most 96 queries leaves softmax warps without a
-    // live row: they write the fused scatter (in place of the index warp)
-    P.idle_scatter = (P.gather && p.fuse_scatter && p.nq <= 96) ? 1 : 0;
     if (P.gather || P.store) {
         ok = ok && map3<D>(&P.mKca, p.Kc, p.N, bh, 64, BN) && map3<D>(&P.mKcb, p.Kc, p.N, bh, tw, BN);
         ok = ok && map3<D>(&P.mVca, p.Vc, p.N, bh, 64, BN) && map3<D>(&P.mVcb, p.Vc, p.N, bh, tw, BN);
@@ -1009,6 +1006,18 @@ cudaError_t launch(const AttnParams &p, cudaStream_t s) {
     const long long tiles = (long long)((p.nq + BM - 1) / BM) * bh;
     if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
     P.n_tiles = (int)tiles;
+    // A single query tile per (b, h) with at most 96 queries leaves softmax warps without a
+    // live row; they write the fused scatter in place of the index warp where that warp's
+    // per-tile work (the bitmap, in-launch copies and the scatter) is a large share of a
+    // tile: short tiles (at most 8 key blocks) and a steady state (at least 4 tiles per CTA).
+    // Measured per call: MAR-H (6 blocks, 27 tiles per CTA) 336 -> 318 us, MAR-L shape
+    // 152 -> 144 us; slower with 18 blocks per tile (512 px, A = 66: 232 -> 243 us) and with
+    // 2.5 tiles per CTA (MAR-B: 33.0 -> 34.9 us).
+    {
+        const int nblk = (p.n_dense + BN - 1) / BN + ((P.gather && p.A < p.N) ? (p.N + BN - 1) / BN : 0);
+        const long long ctas = tiles < 2LL * sm_count() ? tiles : 2LL * sm_count();
+        P.idle_scatter = (P.gather && p.fuse_scatter && p.nq <= 96 && nblk <= 8 && tiles >= 4 * ctas) ? 1 : 0;
+    }
     size_t smem = 1024 + C::oBars + 8 * (KV_FULL + 2 * C::kStages + 2) + 16;
     smem += sizeof(uint32_t) * 2 * 2 * ((p.N + BN - 1) / BN);  // two bitmaps
     const bool gen = p.gen != nullptr && !P.gather;

@@ -613,3 +613,35 @@ def test_cfg_residual(n):
     mar.mar_cfg_residual(mar.MAR_CFG_UPDATE, cond, unc, res2)
     _, r_ref, _ = oracle.cfg(oracle.CFG_UPDATE, cond, uncond=unc)
     assert np.array_equal(res2.cpu().numpy(), r_ref.astype(np.float32))
+
+
+@pytest.mark.parametrize("form", ["gather", "dense"])
+def test_cache_aware_fused_scatter_mar_h_full_size(form):
+    # MAR-H shape (8192 short tiles, many per CTA): the fused scatter is written by the
+    # softmax warps without a live row; the whole cache is bit-exact and sampled rows of the
+    # output match the oracle on the pre-scatter cache
+    cfg = workloads.CONFIGS["mar_h"]
+    A = cfg.A
+    shape = (cfg.Bp, cfg.H, cfg.N, cfg.d)
+    Q, K, V = (_rand(shape, 601 + i, torch.bfloat16) for i in range(3))
+    Kc, Vc = _rand(shape, 605, torch.bfloat16), _rand(shape, 606, torch.bfloat16)
+    Kc0, Vc0 = Kc.clone(), Vc.clone()
+    idx = _active(cfg.Bp, A, cfg.N, 607)
+    st = _status()
+    if form == "gather":
+        O = mar.mar_attn_cache_aware_gather(Q, K, V, Kc, Vc, idx, fuse_scatter=True, status=st)
+    else:
+        QA, KA, VA = (torch.stack([x[b][:, idx[b].long()] for b in range(cfg.Bp)]).contiguous() for x in (Q, K, V))
+        O = mar.mar_attn_cache_aware(QA, KA, VA, Kc, Vc, idx, fuse_scatter=True, status=st)
+    assert mar.mar_status_read(st) == 0
+    rows = [0, 129, cfg.Bp - 1]
+    for b in rows:
+        sl = slice(b, b + 1)
+        QA_, KA_, VA_ = (_gather_host(x[sl], idx[sl]) for x in (Q, K, V))
+        O_ref, _ = oracle.cache_aware(QA_, KA_, VA_, Kc0[sl], Vc0[sl], idx[sl])
+        P.assert_close(O[sl], O_ref, "bf16", f"MAR-H row {b}")
+    want_k, want_v = Kc0, Vc0
+    for b in range(cfg.Bp):
+        want_k[b][:, idx[b].long()] = K[b][:, idx[b].long()]
+        want_v[b][:, idx[b].long()] = V[b][:, idx[b].long()]
+    assert torch.equal(Kc, want_k) and torch.equal(Vc, want_v), "fused scatter"
