@@ -30,7 +30,8 @@
 //              (in the gather form the index warp owns the Q buffers and does both)
 //   warp 5     S issuer (one elected lane):  S_g = Q K_g^T  (M=128, N=64, K=d, K-major
 //              operands), once K_g has landed and PV_{g-SB} has released S/P buffer g % SB;
-//              before a cache block's S, the whole warp clears its stale V rows
+//              as soon as a cache block's stage has landed (before the wait for PV_{g-SB},
+//              which this work then overlaps), the whole warp clears its stale V rows
 //   warp 7     PV issuer (one elected lane): O += P_g V_g  (M=128, N=d, K=64, P from
 //              TMEM, V MN-major), as soon as P_g is written; it releases the K/V stage
 //   warp 6     index warp: bitmap of the active positions of each tile (double-
@@ -40,6 +41,13 @@
 // g numbers the key blocks of a CTA across its tiles; every ring (stages, S/P buffers,
 // Q buffers, bitmaps) is indexed by g or by the tile count, and every barrier is waited
 // one phase at a time, in order, so parity waits are exact.
+//
+// Shared memory: two Q buffers and a ring of K/V stages, 3 for d = 80 and 4 for d = 64, one
+// more when a launch has at most 64 queries (cache-aware attention of up to 64 active rows):
+// its Q buffers then hold 64 rows. At d = 80 with two S/P buffers, the per-block chain
+// P_g -> PV_g -> S_{g+2} is what bounds the softmax warps, and a stage landing late (a
+// stage is reloaded only after the PV of the block it held) lengthens it; the extra stage
+// took the MAR-H cache-aware launch from 295 to 270 us.
 //
 // Tensor memory (256 columns): SB S buffers of 64 columns (three for d = 64, two for
 // d = 80), each overwritten in place by P as packed bf16 pairs, and O (d columns)
@@ -71,14 +79,19 @@ constexpr int kThreads = 256;    // 8 warps
 constexpr uint32_t kTmemCols = 256;
 constexpr float kRescale = 8.f;  // lazy-rescale threshold (base-2 units)
 
-template <int D>
+// QR: query rows a Q buffer holds. 64 for launches of at most 64 queries (the MMAs still
+// read 128 rows: rows 64..127 fall on whatever follows in shared memory, and their S, P and
+// O lanes belong to softmax warps that have no live row and never read them), else BM.
+template <int D, int QR = BM>
 struct Cfg {
     static constexpr int DB = D - 64;                                   // tail columns (0 or 16)
-    static constexpr int kStages = (D == 64) ? 4 : 3;
+    // K/V stages: what shared memory holds next to two Q buffers of QR rows (two CTAs per SM)
+    static constexpr int kStages = ((D == 64) ? 4 : 3) + (QR < BM ? 1 : 0);
+    static_assert(kStages <= 5, "barrier slots hold at most five stages");
     // S/P buffers of 64 tensor-memory columns; O takes D columns after them (<= 256)
     static constexpr int kSB = (D == 64) ? 3 : 2;
     static_assert(64 * kSB + D <= 256, "tensor memory: S/P buffers + O exceed 256 columns");
-    static constexpr uint32_t kQa = BM * 128, kQb = BM * DB * 2;        // Q tile parts
+    static constexpr uint32_t kQa = QR * 128, kQb = QR * DB * 2;        // Q tile parts
     static constexpr uint32_t kQBytes = ((kQa + kQb + 1023) / 1024) * 1024;
     static constexpr uint32_t kKa = BN * 128, kKb = BN * DB * 2;        // one K (or V) block
     static constexpr uint32_t kKV = 2 * (kKa + kKb);                    // K + V of one block
@@ -101,9 +114,9 @@ enum Bar {
     BM_FULL = 13,    // [2]
     BM_EMPTY = 15,   // [2]
     O_STAGED = 17,   // [2] the tile's normalised O is in its Q buffer (one arrival per softmax warp)
-    DENSE_DONE = 19, // [S <= 4] fresh mode: the index warp is done with a dense-block stage
-    DENSE_GO = 23,   // [S] fresh mode: the producer hands a free stage for a dense block to it
-    KV_FULL = 27     // [S], then KV_EMPTY [S]
+    DENSE_DONE = 19, // [S <= 5] fresh mode: the index warp is done with a dense-block stage
+    DENSE_GO = 24,   // [S] fresh mode: the producer hands a free stage for a dense block to it
+    KV_FULL = 29     // [S], then KV_EMPTY [S]
 };
 
 template <int D>
@@ -192,9 +205,9 @@ MAR_DEVINL void st_global_row64_v8_if(bool pred, float *ptr, const float *v) {
 // kGen: 0 = plain attention; 1 = with the generating rows' raw scores, 16-byte stores;
 // 2 = the same with 32-byte stores (N % 8 == 0 and a 32-byte-aligned score buffer, so that
 // every row and block starts on a 32-byte boundary).
-template <int D, int kGen>
+template <int D, int kGen, int QR>
 __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Params<D> P) {
-    using C = Cfg<D>;
+    using C = Cfg<D, QR>;
     constexpr int S = C::kStages;
     constexpr int SB = C::kSB;
     const AttnParams &p = P.a;
@@ -382,13 +395,14 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             const int it = g / nblk, j = g - it * nblk;
             if (!mbar_wait_all(&bars[KV_FULL + g % S], (g / S) & 1, p.status, abort_flag)) break;
             if (j == 0 && !mbar_wait_all(&bars[Q_FULL + (it & 1)], (it >> 1) & 1, p.status, abort_flag)) break;
-            if (g >= SB && !mbar_wait_all(&bars[O_DONE + g % SB], (g / SB - 1) & 1, p.status, abort_flag)) break;
-            tc_fence_after();
             if (j >= nd) {
                 // A cache block: its rows at active positions are stale. Their P will be 0, but
                 // 0 x NaN is NaN, so their V rows are cleared in shared memory here, before S
                 // is issued (PV_g, which reads them, follows S_g through the softmax warps'
                 // hand-over). Whole rows are cleared, so the swizzle inside a row does not matter.
+                // After the clear (stores and proxy fence) this warp's next barrier test took
+                // 700-1000 cycles even on a completed phase (measured); the wait for PV_{g-SB}
+                // below comes after the clear and hides that.
                 if (j == nd && !mbar_wait_all(&bars[BM_FULL + (it & 1)], (it >> 1) & 1, p.status, abort_flag)) break;
                 const uint32_t *bm = bitmaps + (it & 1) * bm_words;
                 const int pos0 = (j - nd) * BN;
@@ -396,18 +410,44 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                 if (p.N - pos0 < 64) stale &= (1ull << (p.N - pos0)) - 1ull;
                 if (stale) {
                     unsigned char *stw = sm + C::oStage + (g % S) * C::kStageBytes;
-                    for (int t = lane; t < BN * 8; t += 32)
-                        if ((stale >> (t >> 3)) & 1ull)
-                            *reinterpret_cast<uint4 *>(stw + C::sVa + 16 * t) = make_uint4(0, 0, 0, 0);
+                    const uint4 z = make_uint4(0, 0, 0, 0);
                     if constexpr (C::DB > 0) {
-                        for (int t = lane; t < BN * 2; t += 32)
-                            if ((stale >> (t >> 1)) & 1ull)
-                                *reinterpret_cast<uint4 *>(stw + C::sVb + 16 * t) = make_uint4(0, 0, 0, 0);
+                        // d = 80 (two S/P buffers: the clear can delay S_g). Lane: 16-byte chunk
+                        // (lane & 7) of rows (lane >> 3) + 4k of part a, chunk (lane & 1) of rows
+                        // (lane >> 1) + 16k of the tail. The tests are shifts and masks of the
+                        // lane's copy of the bits, every store is predicated at a constant offset
+                        // from the lane's base: 20 stores and no loop or bit counts (which would
+                        // take the XU pipe from the softmax's exponentials). Measured with three
+                        // stages: 4% faster on the MAR-H shape than the loop below, which is 2%
+                        // faster at d = 64.
+                        const uint64_t sa = stale >> (lane >> 3);
+                        const uint32_t alo = (uint32_t)sa, ahi = (uint32_t)(sa >> 32);
+                        uint4 *va = reinterpret_cast<uint4 *>(stw + C::sVa) + 8 * (lane >> 3) + (lane & 7);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            if (alo & (1u << (4 * k))) va[32 * k] = z;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            if (ahi & (1u << (4 * k))) va[256 + 32 * k] = z;
+                        const uint64_t sb = stale >> (lane >> 1);
+                        const uint32_t blo = (uint32_t)sb, bhi = (uint32_t)(sb >> 32);
+                        uint4 *vb = reinterpret_cast<uint4 *>(stw + C::sVb) + 2 * (lane >> 1) + (lane & 1);
+                        if (blo & 1u) vb[0] = z;
+                        if (blo & (1u << 16)) vb[32] = z;
+                        if (bhi & 1u) vb[64] = z;
+                        if (bhi & (1u << 16)) vb[96] = z;
+                    } else {
+                        for (int t = lane; t < BN * 8; t += 32)
+                            if ((stale >> (t >> 3)) & 1ull) *reinterpret_cast<uint4 *>(stw + C::sVa + 16 * t) = z;
                     }
                     fence_proxy_async_smem();
                 }
                 __syncwarp();
             }
+            // PV_{g-SB} reads the S/P buffer that S_g overwrites (its stage is not g's: the ring
+            // has more stages than S/P buffers), so the clear above need not wait for it
+            if (g >= SB && !mbar_wait_all(&bars[O_DONE + g % SB], (g / SB - 1) & 1, p.status, abort_flag)) break;
+            tc_fence_after();
             const unsigned char *sq = sm + C::oQ + (it & 1) * C::kQBytes;
             const unsigned char *stg = sm + C::oStage + (g % S) * C::kStageBytes;
             const uint64_t dQa = smem_desc(sq, 16, 1024, Swz::B128);
@@ -973,25 +1013,26 @@ int sm_count() {
     return cache[dev];
 }
 
-template <int D>
+template <int D, int QR>
 cudaError_t launch(const AttnParams &p, cudaStream_t s) {
-    using C = Cfg<D>;
+    using C = Cfg<D, QR>;
     static int configured[64] = {0}, configured_gen[64] = {0}, configured_gen8[64] = {0};
     Tc5Params<D> P;
     P.a = p;
     P.gather = p.idx ? 1 : 0;
     const int bh = p.B * p.H;
     const uint32_t tw = D == 64 ? 64 : 16;  // tail box width (the tail maps are unused for d = 64)
-    bool ok = map3<D>(&P.mOa, p.O, p.nq, bh, 64, BM) && map3<D>(&P.mOb, p.O, p.nq, bh, tw, BM);
+    if (QR < BM && p.nq > QR) return cudaErrorInvalidValue;
+    bool ok = map3<D>(&P.mOa, p.O, p.nq, bh, 64, QR) && map3<D>(&P.mOb, p.O, p.nq, bh, tw, QR);
     if (p.fresh) {
         // the index warp copies the active rows; these maps over the whole fresh tensors are
         // only prefetched, never loaded from
         if (!p.idx || p.nq != p.A || p.n_dense != p.A) return cudaErrorInvalidValue;
-        ok = ok && map3<D>(&P.mQa, p.Q, p.N, bh, 64, BM) && map3<D>(&P.mQb, p.Q, p.N, bh, tw, BM);
+        ok = ok && map3<D>(&P.mQa, p.Q, p.N, bh, 64, QR) && map3<D>(&P.mQb, p.Q, p.N, bh, tw, QR);
         ok = ok && map3<D>(&P.mKa, p.Kd, p.N, bh, 64, BN) && map3<D>(&P.mKb, p.Kd, p.N, bh, tw, BN);
         ok = ok && map3<D>(&P.mVa, p.Vd, p.N, bh, 64, BN) && map3<D>(&P.mVb, p.Vd, p.N, bh, tw, BN);
     } else {
-        ok = ok && map3<D>(&P.mQa, p.Q, p.nq, bh, 64, BM) && map3<D>(&P.mQb, p.Q, p.nq, bh, tw, BM);
+        ok = ok && map3<D>(&P.mQa, p.Q, p.nq, bh, 64, QR) && map3<D>(&P.mQb, p.Q, p.nq, bh, tw, QR);
         ok = ok && map3<D>(&P.mKa, p.Kd, p.n_dense, bh, 64, BN) && map3<D>(&P.mKb, p.Kd, p.n_dense, bh, tw, BN);
         ok = ok && map3<D>(&P.mVa, p.Vd, p.n_dense, bh, 64, BN) && map3<D>(&P.mVb, p.Vd, p.n_dense, bh, tw, BN);
     }
@@ -1022,20 +1063,26 @@ cudaError_t launch(const AttnParams &p, cudaStream_t s) {
     smem += sizeof(uint32_t) * 2 * 2 * ((p.N + BN - 1) / BN);  // two bitmaps
     const bool gen = p.gen != nullptr && !P.gather;
     if (gen && (p.G < 1 || p.G > 32)) return cudaErrorInvalidValue;  // one generating slot per lane
+    if (QR < BM && gen) return cudaErrorInvalidValue;                 // (the score forms use BM rows)
     // 32-byte raw-score stores when every row and block of the score buffer starts on a
     // 32-byte boundary (row starts are multiples of 4 N bytes, block starts of 256 bytes)
     const bool gen8 = gen && (p.N % 8) == 0 && (reinterpret_cast<uintptr_t>(p.gen_s) % 32) == 0;
-    cudaError_t e = gen8  ? ensure_smem(attn_tc5_kernel<D, 2>, smem, configured_gen8, /*max_carveout=*/true)
-                    : gen ? ensure_smem(attn_tc5_kernel<D, 1>, smem, configured_gen, /*max_carveout=*/true)
-                          : ensure_smem(attn_tc5_kernel<D, 0>, smem, configured, /*max_carveout=*/true);
-    if (e != cudaSuccess) return e;
     const long long grid = tiles < 2LL * sm_count() ? tiles : 2LL * sm_count();
-    if (gen8)
-        attn_tc5_kernel<D, 2><<<(unsigned)grid, kThreads, smem, s>>>(P);
-    else if (gen)
-        attn_tc5_kernel<D, 1><<<(unsigned)grid, kThreads, smem, s>>>(P);
-    else
-        attn_tc5_kernel<D, 0><<<(unsigned)grid, kThreads, smem, s>>>(P);
+    if constexpr (QR == BM) {
+        if (gen8 || gen) {
+            cudaError_t e = gen8 ? ensure_smem(attn_tc5_kernel<D, 2, QR>, smem, configured_gen8, /*max_carveout=*/true)
+                                 : ensure_smem(attn_tc5_kernel<D, 1, QR>, smem, configured_gen, /*max_carveout=*/true);
+            if (e != cudaSuccess) return e;
+            if (gen8)
+                attn_tc5_kernel<D, 2, QR><<<(unsigned)grid, kThreads, smem, s>>>(P);
+            else
+                attn_tc5_kernel<D, 1, QR><<<(unsigned)grid, kThreads, smem, s>>>(P);
+            return cudaGetLastError();
+        }
+    }
+    cudaError_t e = ensure_smem(attn_tc5_kernel<D, 0, QR>, smem, configured, /*max_carveout=*/true);
+    if (e != cudaSuccess) return e;
+    attn_tc5_kernel<D, 0, QR><<<(unsigned)grid, kThreads, smem, s>>>(P);
     return cudaGetLastError();
 }
 
@@ -1044,8 +1091,11 @@ cudaError_t launch(const AttnParams &p, cudaStream_t s) {
 bool attn_tc5_supported(const AttnParams &p) { return p.d == 64 || p.d == 80; }
 
 cudaError_t launch_attn_bf16_tc5(const AttnParams &p, cudaStream_t s) {
-    if (p.d == 64) return launch<64>(p, s);
-    if (p.d == 80) return launch<80>(p, s);
+    // launches of at most 64 queries (cache-aware attention of up to 64 active rows) keep
+    // half-height Q buffers and one more K/V stage
+    const bool q64 = p.nq <= 64 && !(p.gen && !p.idx);
+    if (p.d == 64) return launch<64, BM>(p, s);
+    if (p.d == 80) return q64 ? launch<80, 64>(p, s) : launch<80, BM>(p, s);
     return cudaErrorInvalidValue;
 }
 
