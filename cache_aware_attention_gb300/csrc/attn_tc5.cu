@@ -88,6 +88,11 @@ struct Cfg {
     // K/V stages: what shared memory holds next to two Q buffers of QR rows (two CTAs per SM)
     static constexpr int kStages = ((D == 64) ? 4 : 3) + (QR < BM ? 1 : 0);
     static_assert(kStages <= 5, "barrier slots hold at most five stages");
+    // Waits spin at d = 64 (the softmax warps keep pace with the tensor pipe there, and a
+    // warp resuming late from a suspended wait costs its block; measured 5-9% faster) and
+    // suspend at d = 80 (where spinning warps take issue slots from the other CTA's softmax
+    // warps on the same sub-partitions; measured 3% slower).
+    static constexpr bool kSpin = (D == 64);
     // S/P buffers of 64 tensor-memory columns; O takes D columns after them (<= 256)
     static constexpr int kSB = (D == 64) ? 3 : 2;
     static_assert(64 * kSB + D <= 256, "tensor memory: S/P buffers + O exceed 256 columns");
@@ -205,6 +210,13 @@ MAR_DEVINL void st_global_row64_v8_if(bool pred, float *ptr, const float *v) {
 // kGen: 0 = plain attention; 1 = with the generating rows' raw scores, 16-byte stores;
 // 2 = the same with 32-byte stores (N % 8 == 0 and a 32-byte-aligned score buffer, so that
 // every row and block starts on a 32-byte boundary).
+// Warp-wide bounded wait of the attention kernel: suspending (try_wait) or spinning.
+template <bool kSpin>
+__device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity, uint32_t *status, volatile int *abort) {
+    if constexpr (kSpin) return mbar_spin_all(bar, parity, status, abort);
+    else return mbar_wait_all(bar, parity, status, abort);
+}
+
 template <int D, int kGen, int QR>
 __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Params<D> P) {
     using C = Cfg<D, QR>;
@@ -387,14 +399,13 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
         // ------------------------------------------------------------ S issuer
         // S_g = Q K_g^T once K_g has landed, Q of its tile has landed and PV_{g-SB} has
         // released S/P buffer g % SB. The whole warp runs the loop so that every descriptor
-        // is warp-uniform; one elected lane issues each tcgen05 instruction. Waits suspend
-        // the warp rather than poll.
+        // is warp-uniform; one elected lane issues each tcgen05 instruction.
         const uint32_t idS = idesc_bf16(BM, BN, 0, 0);
         const int total = my_tiles * nblk;
         for (int g = 0; g < total; ++g) {
             const int it = g / nblk, j = g - it * nblk;
-            if (!mbar_wait_all(&bars[KV_FULL + g % S], (g / S) & 1, p.status, abort_flag)) break;
-            if (j == 0 && !mbar_wait_all(&bars[Q_FULL + (it & 1)], (it >> 1) & 1, p.status, abort_flag)) break;
+            if (!wait_all<C::kSpin>(&bars[KV_FULL + g % S], (g / S) & 1, p.status, abort_flag)) break;
+            if (j == 0 && !wait_all<C::kSpin>(&bars[Q_FULL + (it & 1)], (it >> 1) & 1, p.status, abort_flag)) break;
             if (j >= nd) {
                 // A cache block: its rows at active positions are stale. Their P will be 0, but
                 // 0 x NaN is NaN, so their V rows are cleared in shared memory here, before S
@@ -403,7 +414,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                 // After the clear (stores and proxy fence) this warp's next barrier test took
                 // 700-1000 cycles even on a completed phase (measured); the wait for PV_{g-SB}
                 // below comes after the clear and hides that.
-                if (j == nd && !mbar_wait_all(&bars[BM_FULL + (it & 1)], (it >> 1) & 1, p.status, abort_flag)) break;
+                if (j == nd && !wait_all<C::kSpin>(&bars[BM_FULL + (it & 1)], (it >> 1) & 1, p.status, abort_flag)) break;
                 const uint32_t *bm = bitmaps + (it & 1) * bm_words;
                 const int pos0 = (j - nd) * BN;
                 uint64_t stale = (uint64_t)bm[pos0 >> 5] | ((uint64_t)bm[(pos0 >> 5) + 1] << 32);
@@ -446,7 +457,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             }
             // PV_{g-SB} reads the S/P buffer that S_g overwrites (its stage is not g's: the ring
             // has more stages than S/P buffers), so the clear above need not wait for it
-            if (g >= SB && !mbar_wait_all(&bars[O_DONE + g % SB], (g / SB - 1) & 1, p.status, abort_flag)) break;
+            if (g >= SB && !wait_all<C::kSpin>(&bars[O_DONE + g % SB], (g / SB - 1) & 1, p.status, abort_flag)) break;
             tc_fence_after();
             const unsigned char *sq = sm + C::oQ + (it & 1) * C::kQBytes;
             const unsigned char *stg = sm + C::oStage + (g % S) * C::kStageBytes;
@@ -482,11 +493,11 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
         const uint32_t idOb = idesc_bf16(BM, 16, 0, 1);
         const int total = my_tiles * nblk;
         for (int g = 0; g < total; ++g) {
-            if (!mbar_wait_all(&bars[P_FULL + g % SB], (g / SB) & 1, p.status, abort_flag)) break;
+            if (!wait_all<C::kSpin>(&bars[P_FULL + g % SB], (g / SB) & 1, p.status, abort_flag)) break;
             // V_g landed long ago (S_g needed the same stage); waiting on its barrier phase
             // here orders this thread's reads after the TMA write. The stage cannot have been
             // refilled: that needs this warp's commit below.
-            if (!mbar_wait_all(&bars[KV_FULL + g % S], (g / S) & 1, p.status, abort_flag)) break;
+            if (!wait_all<C::kSpin>(&bars[KV_FULL + g % S], (g / S) & 1, p.status, abort_flag)) break;
             tc_fence_after();
             const int j = g % nblk;
             const unsigned char *stg = sm + C::oStage + (g % S) * C::kStageBytes;
@@ -599,7 +610,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
         auto build_bitmap = [&](int it, int b) -> bool {
             const int bb = it & 1;
             uint32_t *bm = bitmaps + bb * bm_words;
-            if (nc > 0 && !mbar_wait_all(&bars[BM_EMPTY + bb], ((it >> 1) & 1) ^ 1, p.status, abort_flag)) return false;
+            if (nc > 0 && !wait_all<C::kSpin>(&bars[BM_EMPTY + bb], ((it >> 1) & 1) ^ 1, p.status, abort_flag)) return false;
             for (int w = lane; w < bm_words; w += 32) bm[w] = 0u;
             __syncwarp();
             uint32_t bad = 0;
@@ -619,7 +630,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
         };
         // fresh mode: this warp owns the Q buffers, so it also stores each tile's staged O
         auto store_o6 = [&](int t) -> bool {
-            if (!mbar_wait_all(&bars[O_STAGED + (t & 1)], (t >> 1) & 1, p.status, abort_flag)) return false;
+            if (!wait_all<C::kSpin>(&bars[O_STAGED + (t & 1)], (t >> 1) & 1, p.status, abort_flag)) return false;
             if (lane == 0) {
                 const int tt = (int)blockIdx.x + t * (int)gridDim.x;
                 const int tbh = tt / nqt, tq0 = (tt % nqt) * BM;
@@ -666,7 +677,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                 }
                 for (int j = 0; j < nd; ++j) {
                     const int g = it * nblk + j, st = g % S;
-                    if (!(ok = mbar_wait_all(&bars[DENSE_GO + st], (go_phase >> st) & 1, p.status, abort_flag))) break;
+                    if (!(ok = wait_all<C::kSpin>(&bars[DENSE_GO + st], (go_phase >> st) & 1, p.status, abort_flag))) break;
                     go_phase ^= 1u << st;
                     unsigned char *stg = sm + C::oStage + st * C::kStageBytes;
                     const bf16 *src[2] = {gK, gV};
@@ -820,9 +831,9 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             for (int j = 0; j < nblk; ++j) {
                 const int g = it * nblk + j, buf = g % SB;
                 if (j == nd && nc > 0 &&
-                    !(ok = mbar_wait_all(&bars[BM_FULL + (it & 1)], (it >> 1) & 1, p.status, abort_flag)))
+                    !(ok = wait_all<C::kSpin>(&bars[BM_FULL + (it & 1)], (it >> 1) & 1, p.status, abort_flag)))
                     break;
-                if (!(ok = mbar_wait_all(&bars[S_FULL + buf], (g / SB) & 1, p.status, abort_flag))) break;
+                if (!(ok = wait_all<C::kSpin>(&bars[S_FULL + buf], (g / SB) & 1, p.status, abort_flag))) break;
                 tc_fence_after();
                 // slots of this block that are keys: dense rows below n_dense; cache rows below
                 // N whose position is not active (active positions hold stale cache rows, whose
@@ -898,7 +909,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                         // O holds the tile's sum over earlier blocks; wait for PV_{g-1} and
                         // scale the rows that raised their max (the others use factor 1).
                         // PV_g, which adds this block, is issued only after P_FULL below.
-                        ok = mbar_wait_all(&bars[O_DONE + (g - 1) % SB], ((g - 1) / SB) & 1, p.status, abort_flag);
+                        ok = wait_all<C::kSpin>(&bars[O_DONE + (g - 1) % SB], ((g - 1) / SB) & 1, p.status, abort_flag);
                         if (ok) {
                             tc_fence_after();
 #pragma unroll
@@ -917,7 +928,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                     // (b, h)'s only tile) writes the fused scatter of this dense block from its
                     // stage: the fresh K/V rows of the active positions to the cache. The stage
                     // stays put until the block's PV, which waits for this warp's arrival below.
-                    if (!(ok = mbar_wait_all(&bars[KV_FULL + g % S], (g / S) & 1, p.status, abort_flag))) break;
+                    if (!(ok = wait_all<C::kSpin>(&bars[KV_FULL + g % S], (g / S) & 1, p.status, abort_flag))) break;
                     scatter_idle(sm + C::oStage + (g % S) * C::kStageBytes, bh, j * BN);
                 }
                 tc_fence_before();
@@ -937,7 +948,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             // issued, so the parity wait is exact; MMAs complete in order, so PV_gl's
             // completion covers all of the tile's PVs.
             const int gl = it * nblk + nblk - 1;
-            if (!(ok = mbar_wait_all(&bars[O_DONE + gl % SB], (gl / SB) & 1, p.status, abort_flag))) break;
+            if (!(ok = wait_all<C::kSpin>(&bars[O_DONE + gl % SB], (gl / SB) & 1, p.status, abort_flag))) break;
             tc_fence_after();
             if (live) {
                 // normalised O, staged as bf16 in this tile's Q buffer (free: the tile's last S

@@ -82,6 +82,28 @@ MAR_DEVINL bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *status, vola
 MAR_DEVINL bool mbar_wait_all(uint64_t *bar, uint32_t parity, uint32_t *status, volatile int *abort) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, status, abort));
 }
+// Spin-wait: non-suspending tests (mbarrier.test_wait), bounded by time (about a second
+// of SM clocks) rather than by a poll count. A warp suspended in try_wait can resume some
+// hundreds of cycles after the phase completes; where the waiting warps' issue slots are
+// not needed by others this polls instead (the d = 64 attention kernel: 5-9% faster).
+constexpr long long kSpinCycles = 1ll << 31;
+MAR_DEVINL bool mbar_spin(uint64_t *bar, uint32_t parity, uint32_t *status, volatile int *abort) {
+    const long long t0 = clock64();
+    for (;;) {
+#pragma unroll 1
+        for (int k = 0; k < 32; ++k)
+            if (mbar_test(bar, parity)) return true;
+        if (abort && *abort) return false;
+        if (clock64() - t0 > kSpinCycles) break;
+    }
+    report(status, MAR_STATUS_TIMEOUT);
+    if (abort) *abort = 1;
+    return false;
+}
+// mbar_spin by every lane of a warp with one result for all of them (as mbar_wait_all).
+MAR_DEVINL bool mbar_spin_all(uint64_t *bar, uint32_t parity, uint32_t *status, volatile int *abort) {
+    return __all_sync(0xffffffffu, mbar_spin(bar, parity, status, abort));
+}
 // The same wait on the abort path: it ignores the abort flag (the CTA is unwinding and
 // waits for its own asynchronous copies and MMAs still in flight before it releases the
 // shared and tensor memory they write). Bounded as well; returns false if it gave up.
