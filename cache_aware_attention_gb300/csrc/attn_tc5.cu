@@ -49,12 +49,12 @@
 // stage is reloaded only after the PV of the block it held) lengthens it; the extra stage
 // took the MAR-H cache-aware launch from 295 to 270 us.
 //
-// Tensor memory (256 columns): SB S buffers of 64 columns (three for d = 64, two for
-// d = 80), each overwritten in place by P as packed bf16 pairs, and O (d columns)
-// accumulated across the blocks of a tile. With three buffers S_{g+1} depends only on
-// PV_{g-2}, long complete, so the softmax warps run from block to block without waiting
-// for the tensor pipe. The kGen instantiation (full attention with the layer-2 score)
-// also stores the raw scores and (m, l) of the rows that are generating queries.
+// Tensor memory (256 columns): two S buffers of 64 columns, each overwritten in place by
+// P as packed bf16 pairs, and O (d columns) accumulated across the blocks of a tile. A
+// third buffer (room for it at d = 64) measured no faster for full attention and 4%
+// slower for the MAR-L cache-aware launch. The kGen instantiation (full attention with
+// the layer-2 score) also stores the raw scores and (m, l) of the rows that are
+// generating queries.
 // Online softmax with a lazy rescale: a row keeps the max m used for its P values; a
 // block whose row max exceeds m by more than 8 (base-2 units) raises m and rescales O
 // and l by 2^(m_old - m_new); otherwise P = 2^(s - m) <= 2^8 and nothing is rescaled.
@@ -94,7 +94,7 @@ struct Cfg {
     // warps on the same sub-partitions; measured 3% slower).
     static constexpr bool kSpin = (D == 64);
     // S/P buffers of 64 tensor-memory columns; O takes D columns after them (<= 256)
-    static constexpr int kSB = (D == 64) ? 3 : 2;
+    static constexpr int kSB = 2;
     static_assert(64 * kSB + D <= 256, "tensor memory: S/P buffers + O exceed 256 columns");
     static constexpr uint32_t kQa = QR * 128, kQb = QR * DB * 2;        // Q tile parts
     static constexpr uint32_t kQBytes = ((kQa + kQb + 1023) / 1024) * 1024;
