@@ -493,11 +493,13 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
         const uint32_t idOb = idesc_bf16(BM, 16, 0, 1);
         const int total = my_tiles * nblk;
         for (int g = 0; g < total; ++g) {
-            if (!wait_all<C::kSpin>(&bars[P_FULL + g % SB], (g / SB) & 1, p.status, abort_flag)) break;
-            // V_g landed long ago (S_g needed the same stage); waiting on its barrier phase
-            // here orders this thread's reads after the TMA write. The stage cannot have been
-            // refilled: that needs this warp's commit below.
+            // V_g has landed (or lands before P_g exists: S_g needs the same stage); waiting on
+            // its barrier phase orders this thread's reads after the TMA write. It comes first,
+            // so that only the P_FULL wait (each wait and its vote take a few hundred cycles even
+            // on a completed phase) sits between the softmax's hand-over and PV_g. The stage
+            // cannot have been refilled: that needs this warp's commit below.
             if (!wait_all<C::kSpin>(&bars[KV_FULL + g % S], (g / S) & 1, p.status, abort_flag)) break;
+            if (!wait_all<C::kSpin>(&bars[P_FULL + g % SB], (g / SB) & 1, p.status, abort_flag)) break;
             tc_fence_after();
             const int j = g % nblk;
             const unsigned char *stg = sm + C::oStage + (g % S) * C::kStageBytes;

@@ -446,7 +446,7 @@ cudaError_t launch_partial_d(const ScoreParams &p, cudaStream_t s) {
 
 // Grid (batch row b, chunk of 64 keys), 256 threads: one score group per 64 threads,
 // one key per thread; the groups' sums are merged in group order (see gen_rows.cuh).
-constexpr int kRKeys = 64, kRThreads = kRKeys * kScoreGroups;
+constexpr int kRKeys = 32, kRThreads = kRKeys * kScoreGroups;
 
 __global__ void __launch_bounds__(kRThreads) score_rows_kernel(const float *__restrict__ gen_s,
                                                                const float2 *__restrict__ gen_ml,
