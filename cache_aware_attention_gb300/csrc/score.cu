@@ -444,8 +444,9 @@ cudaError_t launch_partial_d(const ScoreParams &p, cudaStream_t s) {
     }
 }
 
-// Grid (batch row b, chunk of 64 keys), 256 threads: one score group per 64 threads,
-// one key per thread; the groups' sums are merged in group order (see gen_rows.cuh).
+// Grid (batch row b, chunk of 32 keys), 128 threads: one score group per warp, one key
+// per thread; the groups' sums are merged in group order (see gen_rows.cuh). Chunks of 64
+// keys (256 threads) measured 2 us slower per call at the MAR-H shape.
 constexpr int kRKeys = 32, kRThreads = kRKeys * kScoreGroups;
 
 __global__ void __launch_bounds__(kRThreads) score_rows_kernel(const float *__restrict__ gen_s,
