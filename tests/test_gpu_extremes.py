@@ -148,8 +148,9 @@ RESCALES = {"wide", "late_dominant", "cache_dominates", "stale_first_block", "st
 @pytest.mark.parametrize("form", ["dense", "gather"])
 @pytest.mark.parametrize("dtype,d", [("bf16", 64), ("bf16", 80), ("bf16", 32), ("f32", 64)])
 def test_cache_aware_softmax_extremes(case, form, dtype, d):
-    # A <= 64 runs key-split tiles (two halves over alternate key blocks); with A = 64 and
-    # the first cache block all active, the second half's first block is entirely stale
+    # A <= 64 runs with 64-row Q buffers (and, at d = 80, a fourth K/V stage); A = 64 puts
+    # that path's maximum query count in one tile whose first cache block is all stale,
+    # A = 70 the same block with 128-row Q buffers
     B, H, N = 3, 4, 320
     A = {"stale_first_block": 70, "stale_first_block_64": 64}.get(case, 40)
     if dtype == "f32" and case == "wide":

@@ -272,9 +272,11 @@ def test_cache_aware_reports_bad_indices():
 GATHER_CASES = [(1, 2, 64, 8, 32), (2, 3, 300, 70, 64), (2, 2, 320, 40, 80), (1, 2, 100, 100, 64),
                 (2, 2, 50, 1, 128), (1, 1, 1088, 114, 80), (3, 2, 257, 130, 64), (2, 3, 320, 3, 64),
                 (1, 2, 640, 301, 80),
-                # two (b, h) per tile when A <= 64: an odd count leaves the last tile half empty;
-                # A == 64 fills both halves; A == N has no cache block
-                (1, 3, 200, 20, 64), (3, 1, 130, 64, 80), (1, 2, 48, 48, 64), (5, 1, 96, 33, 64)]
+                # the Q buffer height switches at 64 queries (64-row buffers and, at d = 80, a
+                # fourth K/V stage at or below it): A = 64 and 65 on both sides, at both head
+                # dims; A == N has no cache block
+                (1, 3, 200, 20, 64), (3, 1, 130, 64, 80), (2, 2, 200, 65, 80), (2, 1, 130, 64, 64),
+                (1, 2, 48, 48, 64), (5, 1, 96, 33, 64)]
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
