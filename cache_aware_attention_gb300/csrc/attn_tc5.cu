@@ -207,9 +207,6 @@ MAR_DEVINL void st_global_row64_v8_if(bool pred, float *ptr, const float *v) {
         "f"(v[62]), "f"(v[63]));
 }
 
-// kGen: 0 = plain attention; 1 = with the generating rows' raw scores, 16-byte stores;
-// 2 = the same with 32-byte stores (N % 8 == 0 and a 32-byte-aligned score buffer, so that
-// every row and block starts on a 32-byte boundary).
 // Warp-wide bounded wait of the attention kernel: suspending (try_wait) or spinning.
 template <bool kSpin>
 __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity, uint32_t *status, volatile int *abort) {
@@ -217,6 +214,9 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity, uint32_
     else return mbar_wait_all(bar, parity, status, abort);
 }
 
+// kGen: 0 = plain attention; 1 = with the generating rows' raw scores, 16-byte stores;
+// 2 = the same with 32-byte stores (N % 8 == 0 and a 32-byte-aligned score buffer, so that
+// every row and block starts on a 32-byte boundary).
 template <int D, int kGen, int QR>
 __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Params<D> P) {
     using C = Cfg<D, QR>;
