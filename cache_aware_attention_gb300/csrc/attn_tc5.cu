@@ -26,8 +26,9 @@
 //              tiles through one ring of stages, running ahead across tile boundaries;
 //              for full attention with the cache refresh it also stores the K/V blocks of
 //              each (b, h)'s first query tile to the cache (TMA tile stores from the stages);
-//              it stores each tile's O, which the epilogue stages in the tile's Q buffer
-//              (in the gather form the index warp owns the Q buffers and does both)
+//              for full attention it stores each tile's O, which the epilogue stages in
+//              the tile's Q buffer (cache-aware launches write O rows from the softmax
+//              warps; in the gather form the index warp owns the Q buffers)
 //   warp 5     S issuer (one elected lane):  S_g = Q K_g^T  (M=128, N=64, K=d, K-major
 //              operands), once K_g has landed and PV_{g-SB} has released S/P buffer g % SB;
 //              as soon as a cache block's stage has landed (before the wait for PV_{g-SB},
@@ -79,9 +80,10 @@ constexpr int kThreads = 256;    // 8 warps
 constexpr uint32_t kTmemCols = 256;
 constexpr float kRescale = 8.f;  // lazy-rescale threshold (base-2 units)
 
-// QR: query rows a Q buffer holds. 64 for launches of at most 64 queries (the MMAs still
-// read 128 rows: rows 64..127 fall on whatever follows in shared memory, and their S, P and
-// O lanes belong to softmax warps that have no live row and never read them), else BM.
+// QR: query rows a Q buffer holds. 64 for cache-aware launches of at most 64 queries (the
+// MMAs still read 128 rows: rows 64..127 fall on whatever follows in shared memory, and
+// their S, P and O lanes belong to softmax warps that have no live row and never read
+// them), else BM.
 template <int D, int QR = BM>
 struct Cfg {
     static constexpr int DB = D - 64;                                   // tail columns (0 or 16)
@@ -127,7 +129,7 @@ enum Bar {
 template <int D>
 struct Tc5Params {
     CUtensorMap mQa, mQb;    // 3-D [BH, nq, D]: box {64,128,1} (SW128) / {16,128,1} (SW32)
-    CUtensorMap mOa, mOb;    // O, the same layout and boxes (tile stores from the staged Q buffer)
+    CUtensorMap mOa, mOb;    // O, the same layout and boxes (full attention: tile stores from the staged Q buffer)
     CUtensorMap mKa, mKb;    // 3-D [BH, n_dense, D], box {64|16, 64, 1}: all rows / active rows
     CUtensorMap mVa, mVb;
     CUtensorMap mKca, mKcb;  // cache [BH, N, D], box {64|16, 64, 1}: read (cache-aware) or
@@ -217,7 +219,9 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity, uint32_
 // kGen: 0 = plain attention; 1 = with the generating rows' raw scores, 16-byte stores;
 // 2 = the same with 32-byte stores (N % 8 == 0 and a 32-byte-aligned score buffer, so that
 // every row and block starts on a 32-byte boundary).
-template <int D, int kGen, int QR>
+// kDirectO: the softmax warps write O rows straight to global memory (cache-aware launches,
+// whose O is A rows per (b, h)); else O is staged in the tile's Q buffer for a TMA store.
+template <int D, int kGen, int QR, bool kDirectO>
 __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Params<D> P) {
     using C = Cfg<D, QR>;
     constexpr int S = C::kStages;
@@ -307,6 +311,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
             // (In fresh mode the index warp owns the Q buffers and does this.)
             auto store_o = [&](int t) -> bool {
                 if (!mbar_wait(&bars[O_STAGED + (t & 1)], (t >> 1) & 1, p.status, abort_flag)) return false;
+                if constexpr (kDirectO) return true;  // the softmax warps wrote O themselves
                 const int tt = (int)blockIdx.x + t * (int)gridDim.x;
                 const int tbh = tt / nqt, tq0 = (tt % nqt) * BM;
                 const unsigned char *src = sm + C::oQ + (t & 1) * C::kQBytes;
@@ -633,7 +638,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
         // fresh mode: this warp owns the Q buffers, so it also stores each tile's staged O
         auto store_o6 = [&](int t) -> bool {
             if (!wait_all<C::kSpin>(&bars[O_STAGED + (t & 1)], (t >> 1) & 1, p.status, abort_flag)) return false;
-            if (lane == 0) {
+            if (!kDirectO && lane == 0) {
                 const int tt = (int)blockIdx.x + t * (int)gridDim.x;
                 const int tbh = tt / nqt, tq0 = (tt % nqt) * BM;
                 const unsigned char *src = sm + C::oQ + (t & 1) * C::kQBytes;
@@ -961,6 +966,38 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                 const int row = q0 + tid, r = tid;
                 const float inv = 1.f / l;
                 unsigned char *stage = sm + C::oQ + (it & 1) * C::kQBytes;
+                if constexpr (kDirectO) {
+                    // a cache-aware launch: each thread writes its own row of O (160 bytes at
+                    // d = 80) straight to global memory; no staging, proxy fence or TMA store
+                    uint4 *orow = reinterpret_cast<uint4 *>(static_cast<bf16 *>(p.O) + ((int64_t)bh * p.nq + row) * D);
+                    const bool w = row < p.nq;
+                    {
+                        float o[64];
+                        tmem_ld64(lane_addr(tmO, warp, 0), o);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            uint4 u;
+                            u.x = pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv);
+                            u.y = pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
+                            u.z = pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
+                            u.w = pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+                            if (w) orow[c] = u;
+                        }
+                    }
+                    if constexpr (C::DB > 0) {
+                        float o[16];
+                        tmem_ld16(lane_addr(tmO, warp, 64), o);
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            uint4 u;
+                            u.x = pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv);
+                            u.y = pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
+                            u.z = pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
+                            u.w = pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+                            if (w) orow[8 + c] = u;
+                        }
+                    }
+                } else {
                 {  // the 64-column part: one tensor-memory load, eight 16-byte chunks
                     float o[64];
                     tmem_ld64(lane_addr(tmO, warp, 0), o);
@@ -989,11 +1026,12 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                         *reinterpret_cast<uint4 *>(tail + r * 32 + ((c ^ sw) << 4)) = u;
                     }
                 }
+                }
                 if (p.lse && row < p.nq) p.lse[(int64_t)bh * p.nq + row] = (m_use + log2f(l)) * kLn2;
                 if constexpr (kGen)
                     if (is_gen) p.gen_ml[(int64_t)bh * p.G + gslot] = make_float2(m_use, l);
             }
-            fence_proxy_async_smem();  // the staged rows, for the TMA store
+            if constexpr (!kDirectO) fence_proxy_async_smem();  // the staged rows, for the TMA store
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[O_STAGED + (it & 1)]);
             // The next tile's first PV overwrites O only after P of its first block, which
@@ -1029,7 +1067,7 @@ int sm_count() {
 template <int D, int QR>
 cudaError_t launch(const AttnParams &p, cudaStream_t s) {
     using C = Cfg<D, QR>;
-    static int configured[64] = {0}, configured_gen[64] = {0}, configured_gen8[64] = {0};
+    static int configured[64] = {0}, configured_gen[64] = {0}, configured_gen8[64] = {0}, configured_ca[64] = {0};
     Tc5Params<D> P;
     P.a = p;
     P.gather = p.idx ? 1 : 0;
@@ -1083,19 +1121,27 @@ cudaError_t launch(const AttnParams &p, cudaStream_t s) {
     const long long grid = tiles < 2LL * sm_count() ? tiles : 2LL * sm_count();
     if constexpr (QR == BM) {
         if (gen8 || gen) {
-            cudaError_t e = gen8 ? ensure_smem(attn_tc5_kernel<D, 2, QR>, smem, configured_gen8, /*max_carveout=*/true)
-                                 : ensure_smem(attn_tc5_kernel<D, 1, QR>, smem, configured_gen, /*max_carveout=*/true);
+            cudaError_t e = gen8 ? ensure_smem(attn_tc5_kernel<D, 2, QR, false>, smem, configured_gen8, /*max_carveout=*/true)
+                                 : ensure_smem(attn_tc5_kernel<D, 1, QR, false>, smem, configured_gen, /*max_carveout=*/true);
             if (e != cudaSuccess) return e;
             if (gen8)
-                attn_tc5_kernel<D, 2, QR><<<(unsigned)grid, kThreads, smem, s>>>(P);
+                attn_tc5_kernel<D, 2, QR, false><<<(unsigned)grid, kThreads, smem, s>>>(P);
             else
-                attn_tc5_kernel<D, 1, QR><<<(unsigned)grid, kThreads, smem, s>>>(P);
+                attn_tc5_kernel<D, 1, QR, false><<<(unsigned)grid, kThreads, smem, s>>>(P);
+            return cudaGetLastError();
+        }
+        if (!p.idx) {  // full attention: O staged for a TMA store (direct stores measured slower)
+            cudaError_t e = ensure_smem(attn_tc5_kernel<D, 0, QR, false>, smem, configured, /*max_carveout=*/true);
+            if (e != cudaSuccess) return e;
+            attn_tc5_kernel<D, 0, QR, false><<<(unsigned)grid, kThreads, smem, s>>>(P);
             return cudaGetLastError();
         }
     }
-    cudaError_t e = ensure_smem(attn_tc5_kernel<D, 0, QR>, smem, configured, /*max_carveout=*/true);
+    // cache-aware attention (the only kind with QR < BM): O rows written by the softmax warps
+    if (!p.idx) return cudaErrorInvalidValue;
+    cudaError_t e = ensure_smem(attn_tc5_kernel<D, 0, QR, true>, smem, configured_ca, /*max_carveout=*/true);
     if (e != cudaSuccess) return e;
-    attn_tc5_kernel<D, 0, QR><<<(unsigned)grid, kThreads, smem, s>>>(P);
+    attn_tc5_kernel<D, 0, QR, true><<<(unsigned)grid, kThreads, smem, s>>>(P);
     return cudaGetLastError();
 }
 
@@ -1106,7 +1152,7 @@ bool attn_tc5_supported(const AttnParams &p) { return p.d == 64 || p.d == 80; }
 cudaError_t launch_attn_bf16_tc5(const AttnParams &p, cudaStream_t s) {
     // launches of at most 64 queries (cache-aware attention of up to 64 active rows) keep
     // half-height Q buffers and one more K/V stage
-    const bool q64 = p.nq <= 64 && !(p.gen && !p.idx);
+    const bool q64 = p.nq <= 64 && p.idx;
     if (p.d == 64) return launch<64, BM>(p, s);
     if (p.d == 80) return q64 ? launch<80, 64>(p, s) : launch<80, BM>(p, s);
     return cudaErrorInvalidValue;
