@@ -45,10 +45,10 @@
 //
 // Shared memory: two Q buffers and a ring of K/V stages, 3 for d = 80 and 4 for d = 64, one
 // more when a launch has at most 64 queries (cache-aware attention of up to 64 active rows):
-// its Q buffers then hold 64 rows. At d = 80 with two S/P buffers, the per-block chain
-// P_g -> PV_g -> S_{g+2} is what bounds the softmax warps, and a stage landing late (a
-// stage is reloaded only after the PV of the block it held) lengthens it; the extra stage
-// took the MAR-H cache-aware launch from 295 to 270 us.
+// its Q buffers then hold 64 rows. A stage is reloaded only after the PV of the block it
+// held, and a stage landing late delays the S of its block, on which the softmax warps
+// wait: the extra stage took the MAR-H cache-aware launch from 295 to 270 us (d = 80) and
+// the MAR-L one from 119 to 117 us (d = 64).
 //
 // Tensor memory (256 columns): two S buffers of 64 columns, each overwritten in place by
 // P as packed bf16 pairs, and O (d columns) accumulated across the blocks of a tile. A
@@ -1153,7 +1153,7 @@ cudaError_t launch_attn_bf16_tc5(const AttnParams &p, cudaStream_t s) {
     // launches of at most 64 queries (cache-aware attention of up to 64 active rows) keep
     // half-height Q buffers and one more K/V stage
     const bool q64 = p.nq <= 64 && p.idx;
-    if (p.d == 64) return launch<64, BM>(p, s);
+    if (p.d == 64) return q64 ? launch<64, 64>(p, s) : launch<64, BM>(p, s);
     if (p.d == 80) return q64 ? launch<80, 64>(p, s) : launch<80, BM>(p, s);
     return cudaErrorInvalidValue;
 }
