@@ -379,6 +379,12 @@ def run_mine(args, ws, rank, local):
                              "cache-aware attention, condition cache",
         "cpu_baseline": cpu,
         "clocks": clocks.summary(),
+        # The pages' own figures, end to end on whole images with trained models (one H100,
+        # ImageNet 256): context only, not comparable with a per-step kernel figure.
+        "context": {"marche_end_to_end_speedup_over_mar": {"B": 1.57, "L": 1.68, "H": 1.72},
+                    "marche_cache_aware_attention_alone_mar_b": 1.55,
+                    "lazymar_speedup": 2.83,
+                    "source": "MARche (Key Experimental Results; Figure 6 breakdown); LazyMAR (abstract)"},
     }
     if rank == 0:
         print(json.dumps(line))
