@@ -381,10 +381,12 @@ def run_mine(args, ws, rank, local):
         "clocks": clocks.summary(),
         # The pages' own figures, end to end on whole images with trained models (one H100,
         # ImageNet 256): context only, not comparable with a per-step kernel figure.
-        "context": {"marche_end_to_end_speedup_over_mar": {"B": 1.57, "L": 1.68, "H": 1.72},
+        "context": {"marche_end_to_end_speedup_over_mar": {"B": 1.57, "L": 1.68, "H": 1.79},
+                    "marche_speedup_stated_in_the_review": "1.57-1.72x",
                     "marche_cache_aware_attention_alone_mar_b": 1.55,
                     "lazymar_speedup": 2.83,
-                    "source": "MARche (Key Experimental Results; Figure 6 breakdown); LazyMAR (abstract)"},
+                    "source": "MARche notes: Main Results table, Speedup Component Breakdown; the MARche "
+                              "review; LazyMAR notes: main results and ablation (token + condition cache)"},
     }
     if rank == 0:
         print(json.dumps(line))
