@@ -53,7 +53,7 @@ K_SWEEP = (16, 32, 64)
 # keyed by a hash of the kernel's sources so that a capture of an older build is not used
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 KERNEL_SOURCES = {
-    "attn_tc5": ["attn_tc5.cu", "tc5.cuh", "common.cuh", "attn.h", "tma_host.h"],
+    "attn_tc5": ["attn_tc5.cu", "attn_tc5_q96.cu", "tc5.cuh", "common.cuh", "attn.h", "tma_host.h"],
 }
 
 

@@ -62,6 +62,9 @@ cudaError_t launch_attn_bf16_mma(const AttnParams &p, cudaStream_t s);
 // tcgen05/TMEM/TMA kernel (head dim 64 or 80).
 bool attn_tc5_supported(const AttnParams &p);
 cudaError_t launch_attn_bf16_tc5(const AttnParams &p, cudaStream_t s);
+// Cache-aware launches of 65 to 96 queries: 96-row Q buffers and one more K/V stage
+// (attn_tc5_q96.cu).
+cudaError_t launch_attn_bf16_tc5_q96(const AttnParams &p, cudaStream_t s);
 
 // bf16 attention: the tcgen05 kernel where it supports the shape, else the mma.sync one.
 inline cudaError_t launch_attn_bf16(const AttnParams &p, cudaStream_t s) {

@@ -1147,15 +1147,19 @@ cudaError_t launch(const AttnParams &p, cudaStream_t s) {
 
 }  // namespace
 
+// attn_tc5_q96.cu includes this file for the kernel and launch templates only.
+#ifndef MAR_TC5_EXTRA_TU
 bool attn_tc5_supported(const AttnParams &p) { return p.d == 64 || p.d == 80; }
 
 cudaError_t launch_attn_bf16_tc5(const AttnParams &p, cudaStream_t s) {
     // launches of at most 64 queries (cache-aware attention of up to 64 active rows) keep
     // half-height Q buffers and one more K/V stage
     const bool q64 = p.nq <= 64 && p.idx;
+    if (!q64 && p.nq <= 96 && p.idx) return launch_attn_bf16_tc5_q96(p, s);  // 96-row Q buffers
     if (p.d == 64) return q64 ? launch<64, 64>(p, s) : launch<64, BM>(p, s);
     if (p.d == 80) return q64 ? launch<80, 64>(p, s) : launch<80, BM>(p, s);
     return cudaErrorInvalidValue;
 }
+#endif  // MAR_TC5_EXTRA_TU
 
 }  // namespace mar
