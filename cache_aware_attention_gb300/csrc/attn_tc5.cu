@@ -44,8 +44,8 @@
 // one phase at a time, in order, so parity waits are exact.
 //
 // Shared memory: two Q buffers and a ring of K/V stages, 3 for d = 80 and 4 for d = 64, one
-// more when a launch has at most 64 queries (cache-aware attention of up to 64 active rows):
-// its Q buffers then hold 64 rows. A stage is reloaded only after the PV of the block it
+// more when a cache-aware launch has at most 96 queries: its Q buffers then hold 64 or 96
+// rows (the 96-row kernels are compiled in attn_tc5_q96.cu). A stage is reloaded only after the PV of the block it
 // held, and a stage landing late delays the S of its block, on which the softmax warps
 // wait: the extra stage took the MAR-H cache-aware launch from 295 to 270 us (d = 80) and
 // the MAR-L one from 119 to 117 us (d = 64).
@@ -80,10 +80,10 @@ constexpr int kThreads = 256;    // 8 warps
 constexpr uint32_t kTmemCols = 256;
 constexpr float kRescale = 8.f;  // lazy-rescale threshold (base-2 units)
 
-// QR: query rows a Q buffer holds. 64 for cache-aware launches of at most 64 queries (the
-// MMAs still read 128 rows: rows 64..127 fall on whatever follows in shared memory, and
-// their S, P and O lanes belong to softmax warps that have no live row and never read
-// them), else BM.
+// QR: query rows a Q buffer holds. 64 or 96 for cache-aware launches of at most that many
+// queries (the MMAs still read 128 rows: the rows past QR fall on whatever follows in
+// shared memory, and their S, P and O lanes belong to softmax warps that have no live row
+// and never read them), else BM.
 template <int D, int QR = BM>
 struct Cfg {
     static constexpr int DB = D - 64;                                   // tail columns (0 or 16)
@@ -1152,8 +1152,8 @@ cudaError_t launch(const AttnParams &p, cudaStream_t s) {
 bool attn_tc5_supported(const AttnParams &p) { return p.d == 64 || p.d == 80; }
 
 cudaError_t launch_attn_bf16_tc5(const AttnParams &p, cudaStream_t s) {
-    // launches of at most 64 queries (cache-aware attention of up to 64 active rows) keep
-    // half-height Q buffers and one more K/V stage
+    // cache-aware launches of at most 64 (96) queries keep 64-row (96-row) Q buffers and one
+    // more K/V stage
     const bool q64 = p.nq <= 64 && p.idx;
     if (!q64 && p.nq <= 96 && p.idx) return launch_attn_bf16_tc5_q96(p, s);  // 96-row Q buffers
     if (p.d == 64) return q64 ? launch<64, 64>(p, s) : launch<64, BM>(p, s);
