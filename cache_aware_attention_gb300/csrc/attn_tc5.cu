@@ -1104,11 +1104,18 @@ cudaError_t launch(const AttnParams &p, cudaStream_t s) {
     // tile: short tiles (at most 8 key blocks) and a steady state (at least 4 tiles per CTA).
     // Measured per call: MAR-H (6 blocks, 27 tiles per CTA) 336 -> 318 us, MAR-L shape
     // 152 -> 144 us; slower with 18 blocks per tile (512 px, A = 66: 232 -> 243 us) and with
-    // 2.5 tiles per CTA (MAR-B: 33.0 -> 34.9 us).
+    // 2.5 tiles per CTA (MAR-B: 33.0 -> 34.9 us). The idle warps' share is A x d / 8 16-byte
+    // chunks of each of K and V per tile, written in batches behind dependent position loads,
+    // and it delays their hand-over of each dense block: with one idle warp, 20 chunks per lane
+    // (MAR-L shape, A = 80) still measured faster there (167 against 193 us), 30 (MAR-H shape,
+    // A = 96) slower (528 against 422 us), so the share is capped at 24 chunks per lane.
     {
         const int nblk = (p.n_dense + BN - 1) / BN + ((P.gather && p.A < p.N) ? (p.N + BN - 1) / BN : 0);
         const long long ctas = tiles < 2LL * sm_count() ? tiles : 2LL * sm_count();
-        P.idle_scatter = (P.gather && p.fuse_scatter && p.nq <= 96 && nblk <= 8 && tiles >= 4 * ctas) ? 1 : 0;
+        const int idle_warps = 4 - (p.nq + 31) / 32;
+        const bool share_ok = idle_warps > 0 && (long long)p.A * (D / 8) <= 24LL * 32 * idle_warps;
+        P.idle_scatter =
+            (P.gather && p.fuse_scatter && p.nq <= 96 && share_ok && nblk <= 8 && tiles >= 4 * ctas) ? 1 : 0;
     }
     size_t smem = 1024 + C::oBars + 8 * (KV_FULL + 2 * C::kStages + 2) + 16;
     smem += sizeof(uint32_t) * 2 * 2 * ((p.N + BN - 1) / BN);  // two bitmaps
