@@ -617,13 +617,14 @@ def test_cfg_residual(n):
     assert np.array_equal(res2.cpu().numpy(), r_ref.astype(np.float32))
 
 
+@pytest.mark.parametrize("A", [40, 96])
 @pytest.mark.parametrize("form", ["gather", "dense"])
-def test_cache_aware_fused_scatter_mar_h_full_size(form):
-    # MAR-H shape (8192 short tiles, many per CTA): the fused scatter is written by the
-    # softmax warps without a live row; the whole cache is bit-exact and sampled rows of the
-    # output match the oracle on the pre-scatter cache
+def test_cache_aware_fused_scatter_mar_h_full_size(form, A):
+    # MAR-H shape (8192 short tiles, many per CTA): at A = 40 the fused scatter is written by
+    # the softmax warps without a live row, at A = 96 (a single such warp, whose share would
+    # be 30 16-byte chunks per lane) by the index warp; the whole cache is bit-exact and
+    # sampled rows of the output match the oracle on the pre-scatter cache
     cfg = workloads.CONFIGS["mar_h"]
-    A = cfg.A
     shape = (cfg.Bp, cfg.H, cfg.N, cfg.d)
     Q, K, V = (_rand(shape, 601 + i, torch.bfloat16) for i in range(3))
     Kc, Vc = _rand(shape, 605, torch.bfloat16), _rand(shape, 606, torch.bfloat16)

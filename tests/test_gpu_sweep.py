@@ -2,10 +2,11 @@
 the fp64 oracle.
 
 The shapes come from a fixed seed (the same list every run) and spread over the places
-where the tensor-core kernel changes its tiling: the Q-buffer height switches at 64
-queries, the idle-warp scatter at 96 queries, 8 key blocks and 4 tiles per CTA, query
-tiles of 128 rows, ragged key blocks (N not a multiple of 64), A = 1, A = N (no cache
-block) and A just below N. Both head dims of the tensor-core kernel (64, 80) and both
+where the tensor-core kernel changes its tiling: the Q-buffer height switches at 64 and 96
+queries, query tiles of 128 rows, ragged key blocks (N not a multiple of 64), A = 1, A = N
+(no cache block) and A just below N. These shapes are small, so their fused scatter is
+written by the index warp; the path where softmax warps without a live row write it needs
+at least four tiles per CTA and runs in the full-size MAR-H and MAR-L tests and loops. Both head dims of the tensor-core kernel (64, 80) and both
 forms of the cache-aware call (active rows dense, or read in place from the fresh
 tensors) run, with and without the fused cache update; every output is compared with the
 oracle (MARche notes, Key Designs 2: the two partial softmax sums merged by the running
