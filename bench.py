@@ -259,8 +259,10 @@ def run_mine(args, ws, rank, local):
     cfg = config_from_args(args)
     A = cfg.A
     sets = [InputSet(cfg, s, dev) for s in range(N_SETS)]
+    # the caches hold finite values (seeded, as a refresh step leaves them), so the decode step
+    # passes that guarantee to the cache-aware launch (MAR_CA_STALE_FINITE)
     step = DecodeStep(cfg.Bp, cfg.H, cfg.N, cfg.d, max(K_SWEEP + (cfg.K,)), max(cfg.sweep_A + (A, cfg.G + cfg.J + max(K_SWEEP))),
-                      device=dev, max_gen=cfg.G)
+                      device=dev, max_gen=cfg.G, stale_finite=True)
     step.K = cfg.K
     if args.only:
         # profiling aid: one layer-2 select call (fills the score and the active set the
@@ -467,10 +469,15 @@ def step_calls(cfg, step, mar, A=None, K=None):
                                                                active_out=act, workspace=step.workspace),
         "gather": lambda s: mar.mar_kv_gather(list(s.layer3), act, dsts=[qa, ka, va]),
         "cache_aware": lambda s: mar.mar_attn_cache_aware(qa, ka, va, s.cache[0], s.cache[1], act, O_A=oa,
-                                                          fuse_scatter=True),
+                                                          fuse_scatter=True, stale_finite=step.stale_finite),
         "cache_aware_gather": lambda s: mar.mar_attn_cache_aware_gather(s.layer3[0], s.layer3[1], s.layer3[2],
                                                                         s.cache[0], s.cache[1], act, O_A=oa,
-                                                                        fuse_scatter=True),
+                                                                        fuse_scatter=True,
+                                                                        stale_finite=step.stale_finite),
+        # the same launch without the finite-cache guarantee: the stale V rows are zeroed first
+        "cache_aware_gather_zeroed": lambda s: mar.mar_attn_cache_aware_gather(s.layer3[0], s.layer3[1],
+                                                                               s.layer3[2], s.cache[0], s.cache[1],
+                                                                               act, O_A=oa, fuse_scatter=True),
         "attn_full_refresh": lambda s: mar.mar_attn_full_refresh(s.layer3[0], s.layer3[1], s.layer3[2], s.cache[0],
                                                                  s.cache[1], step.O3),
         "cfg": lambda s: mar.mar_cfg_residual(mar.MAR_CFG_APPLY, s.cond, s.uncond, s.residual),
@@ -494,6 +501,7 @@ def step_calls(cfg, step, mar, A=None, K=None):
             "gather": 2 * 3 * cfg.Bp * cfg.H * A * cfg.d * 2,
             "cache_aware": bytes_cache_aware(cfg, A) + bytes_scatter(cfg, A),
             "cache_aware_gather": bytes_cache_aware(cfg, A) + bytes_scatter(cfg, A),
+            "cache_aware_gather_zeroed": bytes_cache_aware(cfg, A) + bytes_scatter(cfg, A),
             "attn_full_refresh": bytes_full_attention(cfg) + 2 * cfg.Bp * cfg.H * cfg.N * cfg.d * 2,
             "cfg": 3 * cfg.B * cfg.n_img * cfg.latent * 4,
             "token_cosine": 2 * cfg.Bp * cfg.H * cfg.N * cfg.d * 2 + cfg.Bp * cfg.N * 4,
@@ -554,7 +562,8 @@ def sweep_active(cfg, sets, step, mar):
         acts = [workloads.distinct_positions(cfg.Bp, A, 0, cfg.N, 880 + 7 * A + s).to(dev) for s in range(N_SETS)]
         oa = step.dense(3, A)
         us = graph_time(lambda i: mar.mar_attn_cache_aware_gather(*sets[i].layer3, *sets[i].cache, acts[i], O_A=oa,
-                                                                  fuse_scatter=True), N_SETS)
+                                                                  fuse_scatter=True, stale_finite=step.stale_finite),
+                        N_SETS)
         b = bytes_cache_aware(cfg, A) + bytes_scatter(cfg, A)
         out[str(A)] = {"active_frac": A / cfg.N, "us": us, "tok_s": cfg.Bp * A / (us * 1e-6),
                        "gbs": b / (us * 1e-6) / 1e9, "hbm_frac": b / (us * 1e-6) / 1e9 / hbm,
@@ -605,7 +614,8 @@ def px512_leg(mar, dev):
         acts = [workloads.distinct_positions(cfg.Bp, A, 0, cfg.N, 4500 + A + s).to(dev) for s in range(2)]
         oa = torch.empty(cfg.Bp, cfg.H, A, cfg.d, dtype=torch.bfloat16, device=dev)
         us_a = graph_time(lambda i: mar.mar_attn_cache_aware_gather(*sets[i][:3], sets[i][3], sets[i][4], acts[i],
-                                                                    O_A=oa, fuse_scatter=True), 2, reps=8)
+                                                                    O_A=oa, fuse_scatter=True, stale_finite=True),
+                          2, reps=8)
         b = bytes_cache_aware(cfg, A) + bytes_scatter(cfg, A)
         out[f"cache_aware_A{A}"] = {"us": us_a, "tok_s": cfg.Bp * A / (us_a * 1e-6), "gbs": b / (us_a * 1e-6) / 1e9,
                                     "hbm_frac": b / (us_a * 1e-6) / 1e9 / hbm}

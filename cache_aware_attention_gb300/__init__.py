@@ -220,10 +220,20 @@ def mar_attn_full_noalloc(Q, K, V, O=None, scale: float = 0.0, gen_idx=None, sco
     return O
 
 
+MAR_CA_FUSE_SCATTER = 0x1
+MAR_CA_STALE_FINITE = 0x2
+
+
+def _ca_flags(fuse_scatter: bool, stale_finite: bool) -> int:
+    return (MAR_CA_FUSE_SCATTER if fuse_scatter else 0) | (MAR_CA_STALE_FINITE if stale_finite else 0)
+
+
 def mar_attn_cache_aware(Q_A, K_A, V_A, K_cache, V_cache, active_idx, O_A=None, scale: float = 0.0,
                          lse_out=None, fuse_scatter: bool = False, workspace=None, status=None,
-                         stream=None):
-    """Split active/cached attention of the A active queries; returns O_A [B,H,A,d]."""
+                         stream=None, stale_finite: bool = False):
+    """Split active/cached attention of the A active queries; returns O_A [B,H,A,d].
+    stale_finite: the caller guarantees finite V_cache rows at the active positions
+    (MAR_CA_STALE_FINITE)."""
     lib = load()
     A = int(Q_A.shape[2])
     s = _shape(Q_A, N=int(K_cache.shape[2]))
@@ -232,17 +242,18 @@ def mar_attn_cache_aware(Q_A, K_A, V_A, K_cache, V_cache, active_idx, O_A=None, 
     wb = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = lib.mar_attn_cache_aware(ctypes.byref(s), A, _ptr(Q_A), _ptr(K_A), _ptr(V_A), _ptr(K_cache),
                                   _ptr(V_cache), _ptr(active_idx), _ptr(O_A), float(scale),
-                                  _ptr(lse_out), int(bool(fuse_scatter)), _ptr(workspace), wb,
+                                  _ptr(lse_out), _ca_flags(fuse_scatter, stale_finite), _ptr(workspace), wb,
                                   _ptr(status), _stream(stream))
     _check("mar_attn_cache_aware", rc)
     return O_A
 
 
 def mar_attn_cache_aware_gather(Q, K, V, K_cache, V_cache, active_idx, O_A=None, scale: float = 0.0,
-                                lse_out=None, fuse_scatter: bool = False, status=None, stream=None):
+                                lse_out=None, fuse_scatter: bool = False, status=None, stream=None,
+                                stale_finite: bool = False):
     """Cache-aware attention of the active rows of the fresh Q/K/V [B,H,N,d], read in place
     through active_idx [B,A] (gather, attention and optional cache update in one launch);
-    returns O_A [B,H,A,d]."""
+    returns O_A [B,H,A,d]. stale_finite as for mar_attn_cache_aware."""
     lib = load()
     A = int(active_idx.shape[1])
     s = _shape(Q)
@@ -250,7 +261,8 @@ def mar_attn_cache_aware_gather(Q, K, V, K_cache, V_cache, active_idx, O_A=None,
         O_A = torch.empty(Q.shape[0], Q.shape[1], A, Q.shape[3], dtype=Q.dtype, device=Q.device)
     rc = lib.mar_attn_cache_aware_gather(ctypes.byref(s), A, _ptr(Q), _ptr(K), _ptr(V), _ptr(K_cache),
                                          _ptr(V_cache), _ptr(active_idx), _ptr(O_A), float(scale),
-                                         _ptr(lse_out), int(bool(fuse_scatter)), _ptr(status), _stream(stream))
+                                         _ptr(lse_out), _ca_flags(fuse_scatter, stale_finite), _ptr(status),
+                                         _stream(stream))
     _check("mar_attn_cache_aware_gather", rc)
     return O_A
 

@@ -198,6 +198,7 @@ int mar_attn_cache_aware_gather(const mar_shape *s, int32_t A, const void *Q, co
     int rc = check_shape(s);
     if (rc != MAR_OK) return rc;
     if (A < 0 || A > s->N) return MAR_ERR_ARG;
+    if (fuse_scatter & ~(MAR_CA_FUSE_SCATTER | MAR_CA_STALE_FINITE)) return MAR_ERR_ARG;
     if (A == 0 || s->B == 0 || s->H == 0) return MAR_OK;
     if (!Q || !K || !V || !K_cache || !V_cache || !active_idx || !O_A) return MAR_ERR_ARG;
     // the cache is written (fused scatter) while the fresh tensors are read: distinct buffers
@@ -213,7 +214,9 @@ int mar_attn_cache_aware_gather(const mar_shape *s, int32_t A, const void *Q, co
     p.Q = Q; p.Kd = K; p.Vd = V; p.Kc = K_cache; p.Vc = V_cache; p.idx = active_idx;
     p.O = O_A; p.lse = lse_out; p.status = d_status;
     p.B = s->B; p.H = s->H; p.N = s->N; p.d = s->d;
-    p.nq = A; p.n_dense = A; p.A = A; p.fuse_scatter = fuse_scatter ? 1 : 0; p.fresh = 1;
+    p.nq = A; p.n_dense = A; p.A = A; p.fresh = 1;
+    p.fuse_scatter = (fuse_scatter & MAR_CA_FUSE_SCATTER) ? 1 : 0;
+    p.stale_finite = (fuse_scatter & MAR_CA_STALE_FINITE) ? 1 : 0;
     p.scale = resolve_scale(scale, s->d);
     cudaError_t e = (s->dtype == MAR_BF16) ? mar::launch_attn_bf16(p, st) : mar::launch_attn_f32(p, st);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -270,6 +273,7 @@ int mar_attn_cache_aware(const mar_shape *s, int32_t A, const void *Q_A, const v
     int rc = check_shape(s);
     if (rc != MAR_OK) return rc;
     if (A < 0 || A > s->N) return MAR_ERR_ARG;
+    if (fuse_scatter & ~(MAR_CA_FUSE_SCATTER | MAR_CA_STALE_FINITE)) return MAR_ERR_ARG;
     if (A == 0 || s->B == 0 || s->H == 0) return MAR_OK;
     if (!Q_A || !K_A || !V_A || !K_cache || !V_cache || !active_idx || !O_A) return MAR_ERR_ARG;
     if (!aligned16(Q_A) || !aligned16(K_A) || !aligned16(V_A) || !aligned16(K_cache) ||
@@ -282,7 +286,9 @@ int mar_attn_cache_aware(const mar_shape *s, int32_t A, const void *Q_A, const v
     p.Q = Q_A; p.Kd = K_A; p.Vd = V_A; p.Kc = K_cache; p.Vc = V_cache; p.idx = active_idx;
     p.O = O_A; p.lse = lse_out; p.status = d_status;
     p.B = s->B; p.H = s->H; p.N = s->N; p.d = s->d;
-    p.nq = A; p.n_dense = A; p.A = A; p.fuse_scatter = fuse_scatter ? 1 : 0;
+    p.nq = A; p.n_dense = A; p.A = A;
+    p.fuse_scatter = (fuse_scatter & MAR_CA_FUSE_SCATTER) ? 1 : 0;
+    p.stale_finite = (fuse_scatter & MAR_CA_STALE_FINITE) ? 1 : 0;
     p.scale = resolve_scale(scale, s->d);
     cudaError_t e = (s->dtype == MAR_BF16) ? mar::launch_attn_bf16(p, st) : mar::launch_attn_f32(p, st);
     if (e != cudaSuccess) return cuda_fail(e);

@@ -30,6 +30,8 @@ struct AttnParams {
     int B, H, N, d;
     int nq, n_dense, A;
     int fuse_scatter;
+    int stale_finite;   // cache-aware: the V cache rows at active positions are finite, so the
+                        // tensor-core kernel need not zero them before P.V (their P is 0)
     int fresh;          // cache-aware only: Q/Kd/Vd are [B*H, N, d], active row a at idx[b, a]
     // Full attention (tcgen05 kernel): the rows of the generating queries gen[b, 0..G) also
     // leave their raw scores and softmax statistics for the layer-2 score (under the first

@@ -415,7 +415,9 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                 // A cache block: its rows at active positions are stale. Their P will be 0, but
                 // 0 x NaN is NaN, so their V rows are cleared in shared memory here, before S
                 // is issued (PV_g, which reads them, follows S_g through the softmax warps'
-                // hand-over). Whole rows are cleared, so the swizzle inside a row does not matter.
+                // hand-over), unless the caller guarantees finite values there (a finite row
+                // times P = 0 adds exactly 0). Whole rows are cleared, so the swizzle inside a
+                // row does not matter.
                 // After the clear (stores and proxy fence) this warp's next barrier test took
                 // 700-1000 cycles even on a completed phase (measured); the wait for PV_{g-SB}
                 // below comes after the clear and hides that.
@@ -424,7 +426,7 @@ __global__ void __maxnreg__(128) attn_tc5_kernel(const __grid_constant__ Tc5Para
                 const int pos0 = (j - nd) * BN;
                 uint64_t stale = (uint64_t)bm[pos0 >> 5] | ((uint64_t)bm[(pos0 >> 5) + 1] << 32);
                 if (p.N - pos0 < 64) stale &= (1ull << (p.N - pos0)) - 1ull;
-                if (stale) {
+                if (stale && !p.stale_finite) {
                     unsigned char *stw = sm + C::oStage + (g % S) * C::kStageBytes;
                     const uint4 z = make_uint4(0, 0, 0, 0);
                     if constexpr (C::DB > 0) {

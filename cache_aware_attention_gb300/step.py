@@ -41,15 +41,20 @@ class DecodeStep:
     b + B'/2 (conditional and unconditional halves of a guidance batch) share one refresh
     set, ranked on the sum of their scores. ``fused_gather``: the cache-aware layer reads its
     active rows in place from the fresh tensors (one launch for gather, attention and cache
-    update) instead of gathering them into dense blocks first."""
+    update) instead of gathering them into dense blocks first. ``stale_finite``: the V caches
+    passed to ``run`` hold finite values (they do once a full-refresh step has written them
+    from finite fresh V, and so does any finite initial cache); the cache-aware launch then
+    uses the stale rows of the active positions as loaded, their weight being exactly 0,
+    instead of zeroing them first (MAR_CA_STALE_FINITE)."""
 
     def __init__(self, B: int, H: int, N: int, d: int, K: int, a_max: int, dtype=torch.bfloat16,
                  device="cuda", max_gen: int | None = None, budget: int | None = None,
-                 shared_pairs: bool = False, fused_gather: bool = True):
+                 shared_pairs: bool = False, fused_gather: bool = True, stale_finite: bool = False):
         if shared_pairs and B % 2:
             raise ValueError("shared_pairs needs an even number of rows")
         self.B, self.H, self.N, self.d, self.K, self.a_max = B, H, N, d, K, a_max
         self.budget, self.shared_pairs, self.fused_gather = budget, shared_pairs, fused_gather
+        self.stale_finite = stale_finite
         self.device = torch.device(device)
         dev, f32, i32 = self.device, torch.float32, torch.int32
         self.score = torch.empty(B, N, dtype=f32, device=dev)
@@ -130,14 +135,14 @@ class DecodeStep:
         if self.fused_gather:
             _record(events, 0, stream)
             mar_attn_cache_aware_gather(Q3, K3, V3, Kc, Vc, act, O_A=oa, fuse_scatter=True, status=self.status,
-                                        stream=stream)
+                                        stream=stream, stale_finite=self.stale_finite)
             _record(events, 1, stream)
             return ("cached", oa, act)
         qa, ka, va = (self.dense(i, A) for i in range(3))
         _record(events, 0, stream)
         mar_kv_gather([Q3, K3, V3], act, dsts=[qa, ka, va], status=self.status, stream=stream)
         mar_attn_cache_aware(qa, ka, va, Kc, Vc, act, O_A=oa, fuse_scatter=True, status=self.status,
-                             stream=stream)
+                             stream=stream, stale_finite=self.stale_finite)
         _record(events, 1, stream)
         return ("cached", oa, act)
 

@@ -80,6 +80,19 @@ enum mar_result {
  * property of the inputs. */
 #define MAR_STATUS_TIMEOUT 0x4u
 
+/* Bits of the `fuse_scatter` argument of mar_attn_cache_aware and
+ * mar_attn_cache_aware_gather (0 and 1 keep their plain meaning; any other bit returns
+ * MAR_ERR_ARG). */
+#define MAR_CA_FUSE_SCATTER 0x1 /* also write K_A/V_A into the cache rows at the active positions */
+/* The caller guarantees that V_cache holds finite values at the active positions, as in a
+ * decode loop, where those rows hold an earlier step's V (written by a refresh or a
+ * scatter). Those rows get attention weight exactly 0 either way. Without this bit the
+ * kernel also zeroes them in shared memory before the P.V product, so that whatever they
+ * hold (NaN or infinity included) leaves the output unchanged; with it they are used as
+ * loaded, and a finite row adds exactly 0. If the guarantee does not hold, the outputs of
+ * the call are unspecified. */
+#define MAR_CA_STALE_FINITE 0x2
+
 enum mar_cfg_mode { MAR_CFG_APPLY = 0, MAR_CFG_UPDATE = 1 };
 
 typedef struct mar_shape {
@@ -218,10 +231,12 @@ int mar_attn_full_noalloc(const mar_shape *shape, const void *Q, const void *K, 
  * concatenated list ([R] Appendix A equivalence).
  *
  *  Q_A, K_A, V_A, O_A  [B,H,A,d]; active_idx [B,A] distinct positions in [0,N).
- *  K_cache, V_cache    [B,H,N,d]. Read at cached positions; when fuse_scatter is
- *                      1 the call also writes K_A/V_A into the rows at the
- *                      active positions (the mar_kv_scatter update), which no
- *                      query of the call reads.
+ *  K_cache, V_cache    [B,H,N,d]. Read at cached positions; with the
+ *                      MAR_CA_FUSE_SCATTER bit of fuse_scatter the call also writes
+ *                      K_A/V_A into the rows at the active positions (the
+ *                      mar_kv_scatter update), which no query of the call reads.
+ *  fuse_scatter        MAR_CA_FUSE_SCATTER | MAR_CA_STALE_FINITE bits (0 or 1 as a
+ *                      plain flag).
  *  lse_out             [B,H,A] fp32 or NULL.
  *  workspace, workspace_bytes
  *                      reserved: the kernels of this call need no scratch memory
@@ -249,8 +264,9 @@ int mar_attn_cache_aware(const mar_shape *shape, int32_t A, const void *Q_A,
  *   Q_A[b,h,a,:] = Q[b,h,active_idx[b,a],:]   (K_A, V_A likewise)
  * and the result is exactly mar_attn_cache_aware(Q_A, K_A, V_A, ...) (the same
  * kernels, reading the rows through active_idx instead of from dense copies).
- * With fuse_scatter = 1 the cache rows at the active positions receive the fresh
- * rows:  K_cache[b,h,p,:] = K[b,h,p,:] for p in active_idx[b] (V likewise).
+ * With the MAR_CA_FUSE_SCATTER bit of fuse_scatter the cache rows at the active
+ * positions receive the fresh rows:  K_cache[b,h,p,:] = K[b,h,p,:] for p in
+ * active_idx[b] (V likewise); MAR_CA_STALE_FINITE as for mar_attn_cache_aware.
  *  Q, K, V             [B,H,N,d] fresh tensors (read only at active positions).
  *  K_cache, V_cache    [B,H,N,d]; must not be the same buffers as K, V or Q.
  *  O_A                 [B,H,A,d];  lse_out [B,H,A] fp32 or NULL.

@@ -101,10 +101,12 @@ def test_attn_full_validation(lib):
 
 def test_cache_aware_validation(lib):
     P = ctypes.c_void_p
-    def call(s, A, idx=FAKE):
+    def call(s, A, idx=FAKE, flags=0):
         return lib.mar_attn_cache_aware(s, A, P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(idx),
-                                        P(FAKE), ctypes.c_float(0), None, 0, None, 0, None, None)
+                                        P(FAKE), ctypes.c_float(0), None, flags, None, 0, None, None)
     assert call(_shape(), 0) == 0            # A == 0 is a no-op
+    assert call(_shape(), 0, flags=4) == -1  # an undefined flag bit
+    assert call(_shape(), 0, flags=8) == -1
     assert call(_shape(), 65) == -1          # A > N
     assert call(_shape(), 8, idx=0) == -1    # NULL idx
     assert call(_shape(d=100), 8) == -2
@@ -181,9 +183,11 @@ def test_attn_full_select_validation(lib):
 
 def test_cache_aware_gather_validation(lib):
     def call(shape, A=8, q=FAKE, k=FAKE + 256, v=FAKE + 512, kc=FAKE + 1024, vc=FAKE + 1280, idx=FAKE + 2048,
-             o=FAKE + 4096):
-        return lib.mar_attn_cache_aware_gather(shape, A, q, k, v, kc, vc, idx, o, 0.0, None, 1, None, None)
+             o=FAKE + 4096, flags=1):
+        return lib.mar_attn_cache_aware_gather(shape, A, q, k, v, kc, vc, idx, o, 0.0, None, flags, None, None)
     assert call(_shape(), A=0) == 0                 # A == 0 is a no-op
+    assert call(_shape(), A=0, flags=3) == 0        # both defined bits
+    assert call(_shape(), A=0, flags=5) == -1       # an undefined flag bit
     assert call(_shape(), A=65) == -1               # A > N
     assert call(_shape(), idx=None) == -1           # NULL positions
     assert call(_shape(), kc=FAKE + 256) == -1      # K cache is the fresh K

@@ -617,13 +617,15 @@ def test_cfg_residual(n):
     assert np.array_equal(res2.cpu().numpy(), r_ref.astype(np.float32))
 
 
+@pytest.mark.parametrize("stale_finite", [False, True])
 @pytest.mark.parametrize("A", [40, 96])
 @pytest.mark.parametrize("form", ["gather", "dense"])
-def test_cache_aware_fused_scatter_mar_h_full_size(form, A):
+def test_cache_aware_fused_scatter_mar_h_full_size(form, A, stale_finite):
     # MAR-H shape (8192 short tiles, many per CTA): at A = 40 the fused scatter is written by
     # the softmax warps without a live row, at A = 96 (a single such warp, whose share would
     # be 30 16-byte chunks per lane) by the index warp; the whole cache is bit-exact and
-    # sampled rows of the output match the oracle on the pre-scatter cache
+    # sampled rows of the output match the oracle on the pre-scatter cache; with stale_finite
+    # the (finite) stale V rows are used as loaded instead of zeroed
     cfg = workloads.CONFIGS["mar_h"]
     shape = (cfg.Bp, cfg.H, cfg.N, cfg.d)
     Q, K, V = (_rand(shape, 601 + i, torch.bfloat16) for i in range(3))
@@ -632,10 +634,12 @@ def test_cache_aware_fused_scatter_mar_h_full_size(form, A):
     idx = _active(cfg.Bp, A, cfg.N, 607)
     st = _status()
     if form == "gather":
-        O = mar.mar_attn_cache_aware_gather(Q, K, V, Kc, Vc, idx, fuse_scatter=True, status=st)
+        O = mar.mar_attn_cache_aware_gather(Q, K, V, Kc, Vc, idx, fuse_scatter=True, status=st,
+                                            stale_finite=stale_finite)
     else:
         QA, KA, VA = (torch.stack([x[b][:, idx[b].long()] for b in range(cfg.Bp)]).contiguous() for x in (Q, K, V))
-        O = mar.mar_attn_cache_aware(QA, KA, VA, Kc, Vc, idx, fuse_scatter=True, status=st)
+        O = mar.mar_attn_cache_aware(QA, KA, VA, Kc, Vc, idx, fuse_scatter=True, status=st,
+                                     stale_finite=stale_finite)
     assert mar.mar_status_read(st) == 0
     rows = [0, 129, cfg.Bp - 1]
     for b in rows:

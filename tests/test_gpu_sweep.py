@@ -95,3 +95,33 @@ def test_full_attention_sweep(B, H, N, A, d, seed):
     O_ref, L_ref = oracle.full_attn(Q.cpu(), K.cpu(), V.cpu())
     P.assert_close(O, O_ref, "bf16", "O full")
     np.testing.assert_allclose(lse.cpu().numpy(), L_ref, atol=2e-4, rtol=0)
+
+
+@pytest.mark.parametrize("form", ["dense", "gather"])
+@pytest.mark.parametrize("B,H,N,A,d,seed", CASES[::3])
+def test_cache_aware_stale_finite_is_bit_identical(B, H, N, A, d, seed, form):
+    # With the caller's guarantee of finite V cache rows at the active positions the kernel
+    # uses those rows as loaded (their weight is exactly 0) instead of zeroing them: every
+    # output and the updated cache are the same bits as without it, and match the oracle
+    t = torch.bfloat16
+    Q, K, V, K0, V0 = (workloads.normal((B, H, N, d), seed + 40 + i, t, DEV) for i in range(5))
+    idx = workloads.distinct_positions(B, A, 0, N, seed + 49).to(DEV)
+    QA, KA, VA = (_gather_host(x, idx) for x in (Q, K, V))
+    res = []
+    for finite in (False, True):
+        Kc, Vc = K0.clone(), V0.clone()
+        lse = torch.empty(B, H, A, dtype=torch.float32, device=DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        if form == "dense":
+            O = mar.mar_attn_cache_aware(QA.to(DEV), KA.to(DEV), VA.to(DEV), Kc, Vc, idx, lse_out=lse,
+                                         fuse_scatter=True, status=st, stale_finite=finite)
+        else:
+            O = mar.mar_attn_cache_aware_gather(Q, K, V, Kc, Vc, idx, lse_out=lse, fuse_scatter=True, status=st,
+                                                stale_finite=finite)
+        assert mar.mar_status_read(st) == 0
+        res.append((P.bits(O), lse.cpu().numpy().view(np.int32), P.bits(Kc), P.bits(Vc)))
+    for a, b in zip(*res):
+        assert np.array_equal(a, b)
+    O_ref, L_ref = oracle.cache_aware(QA, KA, VA, K0.cpu(), V0.cpu(), idx.cpu())
+    P.assert_close(O, O_ref, "bf16", f"O_A {form} finite stale rows")
+    np.testing.assert_allclose(lse.cpu().numpy(), L_ref, atol=2e-4, rtol=0)
